@@ -1,0 +1,124 @@
+/*
+ * fa.h - C ABI of the GB300 (sm_103a) fused tiled attention library.
+ *
+ * Exact scaled-dot-product attention, forward and backward, computed tile by
+ * tile on the GPU without ever writing an N x N matrix to HBM.
+ *
+ * Sources for what is computed:
+ *  - "ELI5: FlashAttention" (A. Gordic), passages on kernel fusion, tiling of
+ *    the N x N scores, the per-row statistics m (maximum) and l (sum of
+ *    exponentials) and their exact merge, and recomputation in the backward.
+ *  - "Potential algorithmic improvements for backward pass" (FlashAttention
+ *    issue 1172): the operand list (Q, K, V, O, log-sum-exp, dO, dV, dK, dQ),
+ *    the 5-GEMM backward with fp32 dQ accumulation, the atomic-free 7-GEMM
+ *    backward (a dK/dV kernel plus a dQ kernel that walks like the forward),
+ *    "implement both and pick what's faster", the 16-byte TMA alignment rule
+ *    and the head-dimension specialisation.
+ *
+ * Definitions (per batch b and head h; rows i, j in [0, N)):
+ *   s_ij  = scale * sum_c Q_ic K_jc,  j visible iff (!causal || j <= i)
+ *   P_ij  = exp(s_ij - LSE_i),        LSE_i = ln sum_{visible j} exp(s_ij)
+ *   O_i   = sum_j P_ij V_j
+ *   D_i   = sum_c dO_ic O_ic
+ *   dS_ij = P_ij (sum_c dO_ic V_jc - D_i)
+ *   dV_j  = sum_i P_ij dO_i,  dQ_i = scale sum_j dS_ij K_j,  dK_j = scale sum_i dS_ij Q_i
+ *
+ * Layout: every matrix argument is a dense, C-contiguous device array of bf16
+ * (raw 16-bit patterns) shaped [B, H, N, d]; LSE is fp32 [B, H, N] holding the
+ * NATURAL log-sum-exp of the SCALED scores.  There are no stride arguments.
+ *
+ * Ownership: the caller allocates and owns every buffer (device memory).  The
+ * library allocates nothing per call; it keeps one lazily created 8-byte
+ * device error word per device for the bounded-wait watchdog.
+ *
+ * Synchronisation: calls only enqueue work on `stream` (a cudaStream_t; NULL
+ * means the legacy default stream) and return at once.  A returned FA_OK means
+ * the launches were accepted; device-side failures are reported by
+ * fa_get_device_error.  Calls on distinct streams may run concurrently.
+ *
+ * Errors: arguments are validated before anything is launched; on any error
+ * nothing is launched and no output is touched.
+ */
+#ifndef TILED_ATTENTION_TMEM_GB300_FA_H_
+#define TILED_ATTENTION_TMEM_GB300_FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FA_OK = 0,
+  FA_ERR_INVALID_ARG = 1,    /* null pointer, negative size, non-finite or non-positive scale */
+  FA_ERR_UNSUPPORTED = 2,    /* head dimension or variant not built for this library */
+  FA_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned (TMA requirement) */
+  FA_ERR_WORKSPACE = 4,      /* workspace NULL or smaller than fa_bwd_workspace_size */
+  FA_ERR_LAUNCH = 5,         /* the CUDA runtime rejected a launch (see fa_last_cuda_error) */
+  FA_ERR_DEVICE_TIMEOUT = 6  /* a bounded in-kernel wait expired; results are invalid */
+} fa_status;
+
+typedef enum {
+  FA_BWD_AUTO = 0,   /* the variant measured fastest for this shape (see fa_bwd_choose) */
+  FA_BWD_5GEMM = 5,  /* one kernel per K/V tile: dK, dV in TMEM, dQ reduced in fp32 */
+  FA_BWD_7GEMM = 7   /* dK/dV kernel + dQ kernel walking like the forward; deterministic */
+} fa_bwd_variant;
+
+/*
+ * Forward.  q, k, v: [B,H,N,d] bf16 (read).  o: [B,H,N,d] bf16 (written).
+ * lse: [B,H,N] fp32 (written), natural log.  d must be 64, 128 or 256.
+ * scale: finite and > 0 (typically 1/sqrt(d)).  causal: 0 or 1 (key j is
+ * visible to query i iff j <= i).  B*H*N == 0 is a no-op returning FA_OK.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, int causal, void* stream);
+
+/*
+ * Bytes of device workspace fa_bwd needs for this shape and variant
+ * (FA_BWD_AUTO: the largest over the variants).  0 for invalid shapes.
+ *   D (fp32 row dot products dO.O):    4*B*H*Npad bytes
+ *   5-GEMM only, fp32 dQ accumulator:  4*B*H*Npad*d bytes
+ * with Npad = N rounded up to a multiple of 128, plus 256 bytes of alignment.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, int variant);
+
+/*
+ * Backward.  Reads q, k, v, o, dO ([B,H,N,d] bf16) and lse ([B,H,N] fp32, as
+ * written by fa_fwd for the same q, k, v, scale, causal); writes dq, dk, dv
+ * ([B,H,N,d] bf16; dq and dk include `scale`).  workspace: device memory of at
+ * least fa_bwd_workspace_size(B,H,N,d,variant) bytes, 256-byte aligned, owned
+ * by the caller and not shared with a concurrent call.  variant: a
+ * fa_bwd_variant value.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, float scale, int causal, int variant,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* The concrete variant (5 or 7) FA_BWD_AUTO runs for this shape. */
+int fa_bwd_choose(int B, int H, int N, int d, int causal);
+
+/*
+ * Synchronises `stream`, then returns FA_ERR_DEVICE_TIMEOUT (and clears the
+ * device error word of the current device) if any kernel of this library on
+ * this device gave up a bounded wait since the last call, FA_ERR_LAUNCH if the
+ * CUDA runtime reports an error, else FA_OK.  `site` (may be NULL) receives
+ * (kernel id << 8) | wait site of the first expired wait.
+ */
+fa_status fa_get_device_error(void* stream, int* site);
+
+/* The last CUDA runtime error code seen by this library on this thread. */
+int fa_last_cuda_error(void);
+
+/* Static description of a status code. */
+const char* fa_strerror(fa_status s);
+
+/* Number of kernels one fa_fwd / fa_bwd call launches for this shape/variant. */
+int fa_fwd_launches(int B, int H, int N, int d);
+int fa_bwd_launches(int B, int H, int N, int d, int variant, int causal);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILED_ATTENTION_TMEM_GB300_FA_H_ */

@@ -1,0 +1,51 @@
+"""Shared test helpers: host<->device marshalling and tolerance checks."""
+
+from __future__ import annotations
+
+import numpy as np
+
+from tiled_attention_tmem_gb300 import inputs as I
+
+# Tolerances stated for this method: O max abs error <= 1e-2, LSE max abs error
+# <= 1e-3, dQ/dK/dV max abs error <= 2e-2 * max|ref| (per tensor).
+TOL_O = 1e-2
+TOL_LSE = 1e-3
+TOL_GRAD_REL = 2e-2
+
+
+def to_dev(bits, device="cuda:0"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def to_f64(t) -> np.ndarray:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return I.bf16_bits_to_f64(t.view(torch.int16).cpu().numpy().view(np.uint16))
+    return t.double().cpu().numpy()
+
+
+def max_abs(a, b) -> float:
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    if not np.all(np.isfinite(a)):
+        return float("inf")
+    return float(np.max(np.abs(a - b))) if a.size else 0.0
+
+
+def check_fwd(o, lse, o_ref, lse_ref, what=""):
+    eo = max_abs(o, o_ref)
+    el = max_abs(lse, lse_ref)
+    assert eo <= TOL_O, f"{what} O max abs err {eo:.3e} > {TOL_O}"
+    assert el <= TOL_LSE, f"{what} LSE max abs err {el:.3e} > {TOL_LSE}"
+    return eo, el
+
+
+def check_grads(got, ref, what=""):
+    out = []
+    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
+        scale = float(np.max(np.abs(r))) if r.size else 0.0
+        e = max_abs(g, r)
+        assert e <= TOL_GRAD_REL * scale, f"{what} {name} max abs err {e:.3e} > {TOL_GRAD_REL}*{scale:.3e}"
+        out.append(e / scale if scale else 0.0)
+    return out

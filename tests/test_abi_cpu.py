@@ -1,0 +1,118 @@
+"""The C-ABI library loads, exports every declared symbol, and validates arguments.
+
+These tests need no GPU: every call below is rejected (or is a no-op) before
+any CUDA work is issued.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tiled_attention_tmem_gb300 import binding as b
+from tiled_attention_tmem_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build_library()
+    return b.lib()
+
+
+def declared_functions():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"\b(fa_[a-z0-9_]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "fa_fwd" in names and "fa_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+        assert n in b.SIGNATURES, f"binding lacks {n}"
+
+
+A = 1 << 20  # a 16-byte aligned fake address; never dereferenced
+
+
+def test_fwd_validation(lib):
+    ok = dict(B=1, H=2, N=128, d=64, scale=0.125, causal=0)
+
+    def call(q=A, k=A, v=A, o=A, lse=A, **kw):
+        a = {**ok, **kw}
+        return b.fa_fwd(q, k, v, o, lse, a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"], None)
+
+    assert call(d=96) == b.FA_ERR_UNSUPPORTED
+    assert call(d=32) == b.FA_ERR_UNSUPPORTED
+    assert call(N=-1) == b.FA_ERR_INVALID_ARG
+    assert call(scale=0.0) == b.FA_ERR_INVALID_ARG
+    assert call(scale=-0.5) == b.FA_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == b.FA_ERR_INVALID_ARG
+    assert call(scale=float("inf")) == b.FA_ERR_INVALID_ARG
+    assert call(causal=2) == b.FA_ERR_INVALID_ARG
+    assert call(q=0) == b.FA_ERR_INVALID_ARG
+    assert call(lse=0) == b.FA_ERR_INVALID_ARG
+    assert call(k=A + 8) == b.FA_ERR_MISALIGNED
+    assert call(lse=A + 4) == b.FA_ERR_MISALIGNED
+    # Empty problems are a no-op and never touch the (null) pointers.
+    assert call(q=0, k=0, v=0, o=0, lse=0, N=0) == b.FA_OK
+    assert call(q=0, k=0, v=0, o=0, lse=0, B=0) == b.FA_OK
+
+
+def test_bwd_validation(lib):
+    ws = b.fa_bwd_workspace_size(1, 2, 128, 64, b.FA_BWD_AUTO)
+    assert ws > 0
+
+    def call(variant=b.FA_BWD_7GEMM, workspace=A, wsb=ws, d=64, scale=0.125, dq=A, lse=A):
+        return b.fa_bwd(A, A, A, A, A, lse, dq, A, A, 1, 2, 128, d, scale, 0, variant,
+                        workspace, wsb, None)
+
+    assert call(variant=3) == b.FA_ERR_INVALID_ARG
+    assert call(d=80) == b.FA_ERR_UNSUPPORTED
+    assert call(scale=0.0) == b.FA_ERR_INVALID_ARG
+    assert call(dq=0) == b.FA_ERR_INVALID_ARG
+    assert call(dq=A + 2) == b.FA_ERR_MISALIGNED
+    if b.lib().fa_bwd_launches(1, 2, 128, 64, b.FA_BWD_7GEMM, 0) > 0:
+        assert call(workspace=0) == b.FA_ERR_WORKSPACE
+        assert call(workspace=A + 16) == b.FA_ERR_WORKSPACE
+        assert call(wsb=ws - 1 - 256 * 0 - 300) == b.FA_ERR_WORKSPACE
+
+
+def test_workspace_sizes(lib):
+    for d in (64, 128, 256):
+        w7 = b.fa_bwd_workspace_size(2, 3, 300, d, b.FA_BWD_7GEMM)
+        assert w7 >= 4 * 6 * 384
+        wa = b.fa_bwd_workspace_size(2, 3, 300, d, b.FA_BWD_AUTO)
+        assert wa >= w7
+        if b.lib().fa_bwd_launches(2, 3, 300, d, b.FA_BWD_5GEMM, 0) > 0:
+            w5 = b.fa_bwd_workspace_size(2, 3, 300, d, b.FA_BWD_5GEMM)
+            assert w5 >= 4 * 6 * 384 * (d + 1)
+    assert b.fa_bwd_workspace_size(1, 1, 128, 100, b.FA_BWD_AUTO) == 0
+    assert b.fa_bwd_workspace_size(1, 1, 128, 64, 9) == 0
+
+
+def test_strerror(lib):
+    for s in range(7):
+        assert b.fa_strerror(s)
+    assert b.fa_strerror(99) == "unknown status"
+
+
+def test_launch_counts(lib):
+    assert b.fa_fwd_launches(1, 1, 0, 64) == 0
+    assert b.fa_fwd_launches(1, 1, 128, 64) == 1
+
+
+def test_no_cpu_fallback_when_library_missing(tmp_path, monkeypatch):
+    """The binding raises instead of computing anything when the .so is absent."""
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(b, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        b.fa_fwd(A, A, A, A, A, 1, 1, 128, 64, 0.125, 0, None)

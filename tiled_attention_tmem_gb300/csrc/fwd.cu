@@ -1,0 +1,58 @@
+// Forward launcher: tile configuration per head dimension and TMA descriptors.
+#include "fwd.cuh"
+#include "host.h"
+
+namespace fa {
+namespace {
+
+// Per head dimension: query tiles per CTA, keys per tile, K/V ring depth.
+//  d = 64 : 2 x 128 query rows, 128 keys, 6 stages (Q 32 KiB + ring 96 KiB)
+//  d = 128: 2 x 128 query rows, 128 keys, 4 stages (Q 64 KiB + ring 128 KiB)
+//  d = 256: 1 x 128 query rows, 128 keys, 2 stages (Q 64 KiB + ring 128 KiB)
+using Fwd64 = FwdCfg<64, 2, 128, 6>;
+using Fwd128 = FwdCfg<128, 2, 128, 4>;
+using Fwd256 = FwdCfg<256, 1, 128, 2>;
+
+template <class C>
+fa_status run(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
+              float scale, int causal, cudaStream_t st) {
+  FwdParams p;
+  fa_status s;
+  if ((s = make_tile_map(&p.q_map, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C::D, N, BH, 64, 128,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) != FA_OK)
+    return s;
+  if ((s = make_tile_map(&p.k_map, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C::D, N, BH, 64, C::BN,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) != FA_OK)
+    return s;
+  if ((s = make_tile_map(&p.v_map, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C::D, N, BH, 64, C::BN,
+                         CU_TENSOR_MAP_SWIZZLE_128B)) != FA_OK)
+    return s;
+  p.o = static_cast<uint16_t*>(o);
+  p.lse = lse;
+  p.err = device_error_word();
+  if (!p.err) return record_cuda_error(cudaErrorMemoryAllocation);
+  p.N = N;
+  p.BH = BH;
+  p.scale_log2 = scale * kLog2e;
+  p.causal = causal;
+  const int n_qblk = (N + 128 * C::NQ - 1) / (128 * C::NQ);
+  const long long blocks = (long long)n_qblk * BH;
+  if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  return launch(fwd_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);
+}
+
+}  // namespace
+
+fa_status run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
+                  int d, float scale, int causal, cudaStream_t st) {
+  switch (d) {
+    case 64: return run<Fwd64>(q, k, v, o, lse, BH, N, scale, causal, st);
+    case 128: return run<Fwd128>(q, k, v, o, lse, BH, N, scale, causal, st);
+    case 256: return run<Fwd256>(q, k, v, o, lse, BH, N, scale, causal, st);
+  }
+  return FA_ERR_UNSUPPORTED;
+}
+
+int fwd_launch_count(int) { return 1; }
+
+}  // namespace fa

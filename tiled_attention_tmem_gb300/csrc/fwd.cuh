@@ -1,0 +1,375 @@
+// Fused attention forward: O = softmax(scale * Q K^T) V and the per-row
+// log-sum-exp, with no N x N matrix in HBM.
+//
+// Method ("ELI5: FlashAttention", tiling and softmax-statistics passages): the
+// score matrix is cut into tiles; each query row keeps a running maximum m and
+// exponential sum l, and partial results are merged with the normalising
+// factor exp(m_old - m_new).  Here the running maximum is kept in the log2
+// domain (scores are multiplied by scale*log2(e) so exp becomes ex2), and the
+// accumulated O is only rescaled when the row maximum grew by more than 8
+// (a factor 256): between rescales the probabilities are computed against the
+// stale maximum, which is exact in arithmetic and keeps every p <= 256.
+//
+// CTA = NQ query tiles of 128 rows sharing one stream of K/V tiles (BN keys).
+//   warp 0        TMA producer: Q tiles once, then K_j, V_j through a ring of
+//                 STAGES shared-memory slots (mbarrier full/empty pairs)
+//   warp 1        TMEM allocator and single-thread tcgen05.mma issuer:
+//                 S_t = Q_t K_j^T (both K-major, smem x smem -> TMEM) and
+//                 O_t += P_t V_j (P from TMEM, V MN-major from smem)
+//   warps 4..     one warpgroup per query tile; thread r owns row r of the tile
+//                 (TMEM lane r), so row max / row sum need no shuffles; P is
+//                 written back as bf16 into the columns of S (tcgen05.st)
+// The MMA issue order S_0(0) S_1(0) PV_0(0) S_0(1) PV_1(0) S_1(1) ... lets the
+// tensor core work on one tile while the other tile's softmax runs.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace fa {
+
+struct FwdParams {
+  CUtensorMap q_map;  // 3-D {d, N, B*H} bf16, box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap k_map;  // same tensor shape, box {64, BN, 1}
+  CUtensorMap v_map;
+  uint16_t* o;  // bf16 [B*H, N, d]
+  float* lse;   // fp32 [B*H, N]
+  int* err;
+  int N;
+  int BH;
+  float scale_log2;  // scale * log2(e)
+  int causal;
+};
+
+template <int D_, int NQ_, int BN_, int STAGES_>
+struct FwdCfg {
+  static constexpr int D = D_, NQ = NQ_, BN = BN_, STAGES = STAGES_;
+  static constexpr int BM = 128;
+  static constexpr int PANELS = D / 64;
+  static constexpr uint32_t Q_PANEL = BM * 128;
+  static constexpr uint32_t Q_TILE = PANELS * Q_PANEL;
+  static constexpr uint32_t KV_PANEL = BN * 128;
+  static constexpr uint32_t KV_TILE = PANELS * KV_PANEL;
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_KV = OFF_Q + NQ * Q_TILE;
+  static constexpr uint32_t OFF_BAR = OFF_KV + STAGES * KV_TILE;
+  // barriers: q_full, kv_full[S], kv_empty[S], s_full[NQ], p_ready[NQ], o_ready[NQ], done
+  static constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES,
+                       B_SFULL = 1 + 2 * STAGES, B_PREADY = B_SFULL + NQ,
+                       B_OREADY = B_PREADY + NQ, B_DONE = B_OREADY + NQ, NBAR = B_DONE + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+  static constexpr int TMEM_S = 0;         // S_t (and P_t aliased) at t*BN
+  static constexpr int TMEM_O = NQ * BN;   // O_t at TMEM_O + t*D
+  static constexpr int TMEM_USED = NQ * (BN + D);
+  static constexpr uint32_t TMEM_COLS =
+      TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
+  static constexpr int THREADS = 128 + 128 * NQ;
+  static_assert(TMEM_USED <= 512, "TMEM budget");
+  static_assert(BN % 32 == 0 && BN <= 256 && D % 64 == 0 && D <= 256, "tile shape");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ int fwd_kv_tiles(int qrow0, int N, int causal, int BN) {
+  if (qrow0 >= N) return 0;
+  if (!causal) return (N + BN - 1) / BN;
+  const int last = min(qrow0 + 127, N - 1);
+  return last / BN + 1;
+}
+
+// Bounded wait used only while draining in-flight copies at teardown; it does
+// not give up early when the CTA is aborting.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_test(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return;
+  }
+}
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
+  constexpr int D = C::D, NQ = C::NQ, BN = C::BN, S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw_addr);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    *abort_flag = (*reinterpret_cast<volatile int*>(p.err) != 0) ? 1 : 0;
+    mbar_init(bar0 + 8 * C::B_QFULL, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar0 + 8 * (C::B_KVFULL + s), 1);
+      mbar_init(bar0 + 8 * (C::B_KVEMPTY + s), 1);
+    }
+    for (int t = 0; t < NQ; ++t) {
+      mbar_init(bar0 + 8 * (C::B_SFULL + t), 1);
+      mbar_init(bar0 + 8 * (C::B_PREADY + t), 4);
+      mbar_init(bar0 + 8 * (C::B_OREADY + t), 1);
+    }
+    mbar_init(bar0 + 8 * C::B_DONE, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const CtaAbort ab{abort_flag, p.err};
+
+  // Tile coordinates: causal launches walk query blocks from the last (the most
+  // key tiles) to the first so the longest CTAs start first.
+  const int n_qblk = (p.N + 128 * NQ - 1) / (128 * NQ);
+  int qb = blockIdx.x / p.BH;
+  const int bh = blockIdx.x % p.BH;
+  if (p.causal) qb = n_qblk - 1 - qb;
+  const int q0 = qb * 128 * NQ;
+  int nkv[NQ];
+  int nmax = 0;
+#pragma unroll
+  for (int t = 0; t < NQ; ++t) {
+    nkv[t] = fwd_kv_tiles(q0 + 128 * t, p.N, p.causal, BN);
+    nmax = max(nmax, nkv[t]);
+  }
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+
+  if (!*abort_flag) {
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        tma_prefetch_desc(&p.q_map);
+        tma_prefetch_desc(&p.k_map);
+        tma_prefetch_desc(&p.v_map);
+        mbar_expect_tx(BAR(C::B_QFULL), NQ * C::Q_TILE);
+        for (int t = 0; t < NQ; ++t)
+          for (int pn = 0; pn < C::PANELS; ++pn)
+            tma_load_3d(sbase + C::OFF_Q + t * C::Q_TILE + pn * C::Q_PANEL, &p.q_map,
+                        BAR(C::B_QFULL), 64 * pn, q0 + 128 * t, bh);
+        int it = 0;
+        bool ok = true;
+        for (int j = 0; j < nmax && ok; ++j) {
+          for (int w = 0; w < 2; ++w) {
+            const int s = it % S;
+            if (!wait_one(BAR(C::B_KVEMPTY + s), ((it / S) & 1) ^ 1, ab, (kKFwd << 8) | 1)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(BAR(C::B_KVFULL + s), C::KV_TILE);
+            const CUtensorMap* m = w ? &p.v_map : &p.k_map;
+            for (int pn = 0; pn < C::PANELS; ++pn)
+              tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m,
+                          BAR(C::B_KVFULL + s), 64 * pn, j * BN, bh);
+            ++it;
+          }
+        }
+        // Let every copy this thread started land before the CTA can exit.
+        wait_drain(BAR(C::B_QFULL), 0);
+        for (int i = max(0, it - S); i < it; ++i) wait_drain(BAR(C::B_KVFULL + i % S), (i / S) & 1);
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issue
+      if (lane == 0) {
+        constexpr uint32_t idS = make_idesc(128, BN, false, false);
+        constexpr uint32_t idO = make_idesc(128, D, false, true);
+        auto issue_s = [&](int t, int s) {
+          const uint32_t qa = sbase + C::OFF_Q + t * C::Q_TILE;
+          const uint32_t kb = sbase + C::OFF_KV + s * C::KV_TILE;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss(tmem + C::TMEM_S + t * BN, desc_kmajor(qa, C::Q_PANEL, 16 * k),
+                   desc_kmajor(kb, C::KV_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+          mma_commit(BAR(C::B_SFULL + t));
+        };
+        bool ok = wait_one(BAR(C::B_QFULL), 0, ab, (kKFwd << 8) | 2);
+        int it = 0;
+        if (ok && nmax > 0) {
+          const int s = it % S;
+          ok = wait_one(BAR(C::B_KVFULL + s), (it / S) & 1, ab, (kKFwd << 8) | 3);
+          if (ok) {
+            tc_fence_after();
+            for (int t = 0; t < NQ; ++t)
+              if (nkv[t] > 0) issue_s(t, s);
+            mma_commit(BAR(C::B_KVEMPTY + s));
+            ++it;
+          }
+        }
+        for (int j = 0; ok && j < nmax; ++j) {
+          const int sv = it % S;
+          ok = wait_one(BAR(C::B_KVFULL + sv), (it / S) & 1, ab, (kKFwd << 8) | 4);
+          ++it;
+          if (!ok) break;
+          tc_fence_after();
+          const int sk = it % S;
+          bool k_ready = false;
+          const uint32_t vb = sbase + C::OFF_KV + sv * C::KV_TILE;
+          for (int t = 0; t < NQ && ok; ++t) {
+            if (j < nkv[t]) {
+              if (!wait_one(BAR(C::B_PREADY + t), j & 1, ab, (kKFwd << 8) | 5)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+#pragma unroll
+              for (int k = 0; k < BN / 16; ++k)
+                mma_ts(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * BN + 8 * k,
+                       desc_mnmajor(vb, C::KV_PANEL, 16 * k), idO, (j > 0 || k > 0) ? 1u : 0u);
+              mma_commit(BAR(C::B_OREADY + t));
+            }
+            if (j + 1 < nkv[t]) {
+              if (!k_ready) {
+                if (!wait_one(BAR(C::B_KVFULL + sk), (it / S) & 1, ab, (kKFwd << 8) | 6)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                k_ready = true;
+              }
+              issue_s(t, sk);
+            }
+          }
+          if (!ok) break;
+          mma_commit(BAR(C::B_KVEMPTY + sv));
+          if (k_ready) {
+            mma_commit(BAR(C::B_KVEMPTY + sk));
+            ++it;
+          }
+        }
+        // Every MMA issued above must finish before TMEM is released.
+        mma_commit(BAR(C::B_DONE));
+        wait_drain(BAR(C::B_DONE), 0);
+      }
+      __syncwarp();
+    } else if (warp >= 4) {
+      // ------------------------------------------------------------ softmax
+      const int t = (warp - 4) >> 2;
+      const int quad = warp & 3;
+      const int r = quad * 32 + lane;
+      const int qi = q0 + 128 * t + r;
+      const int n = nkv[t];
+      const int limit = p.causal ? min(qi, p.N - 1) : p.N - 1;
+      const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+      const uint32_t tS = trow + C::TMEM_S + t * BN;
+      const uint32_t tO = trow + C::TMEM_O + t * D;
+      const float cs = p.scale_log2;
+      float m_used = -INFINITY;
+      float l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        if (!wait_warp(BAR(C::B_SFULL + t), j & 1, ab, (kKFwd << 8) | 7)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[BN];
+#pragma unroll
+        for (int c = 0; c < BN; c += 32) tmem_ld_32x32b_x32(tS + c, sr + c);
+        tmem_wait_ld();
+        reg_fence<BN>(sr);
+        const int kbase = j * BN;
+        if (kbase + BN - 1 > limit) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (kbase + c > limit) sr[c] = __float_as_uint(-INFINITY);
+        }
+        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < BN; c += 4) {
+          mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
+          mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
+          mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
+          mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+        }
+        const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs;
+        const bool need = m_cand > m_used + 8.0f;
+        float alpha = 1.f;
+        if (need) {
+          alpha = ex2(m_used - m_cand);
+          m_used = m_cand;
+          l *= alpha;
+        }
+        const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+        float l0 = 0.f, l1 = 0.f;
+#pragma unroll
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[c + e]), cs, -msub));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[c + e + 1]), cs, -msub));
+            l0 += p0;
+            l1 += p1;
+            pk[e >> 1] = pack_bf16(p0, p1);
+          }
+          tmem_st_32x32b_x16(tS + (c >> 1), pk);
+        }
+        l += l0 + l1;
+        tmem_wait_st();
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // Rescale the running O once the MMA that last accumulated into it is done.
+          if (!wait_warp(BAR(C::B_OREADY + t), (j - 1) & 1, ab, (kKFwd << 8) | 8)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t orr[32];
+            tmem_ld_32x32b_x32(tO + c0, orr);
+            tmem_wait_ld();
+            reg_fence<32>(orr);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+            tmem_st_32x32b_x32(tO + c0, orr);
+          }
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(C::B_PREADY + t));
+      }
+      if (ok && n > 0) {
+        if (wait_warp(BAR(C::B_OREADY + t), (n - 1) & 1, ab, (kKFwd << 8) | 9)) {
+          tc_fence_after();
+          const float inv = 1.f / l;
+          const bool store = qi < p.N;
+          uint16_t* orow = p.o + ((size_t)bh * p.N + (size_t)(store ? qi : 0)) * D;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t orr[32];
+            tmem_ld_32x32b_x32(tO + c0, orr);
+            tmem_wait_ld();
+            reg_fence<32>(orr);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              pk[e >> 1] = pack_bf16(__uint_as_float(orr[e]) * inv, __uint_as_float(orr[e + 1]) * inv);
+            if (store) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+          }
+          if (store) p.lse[(size_t)bh * p.N + qi] = (m_used + log2f(l)) * kLn2;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace fa

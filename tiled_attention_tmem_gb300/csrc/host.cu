@@ -1,0 +1,192 @@
+// C ABI entry points: argument validation, workspace sizing, device error word,
+// variant choice, and dispatch to the kernel launchers.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "fa.h"
+#include "host.h"
+
+namespace fa {
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+std::mutex g_mutex;
+constexpr int kMaxDevices = 64;
+int* g_err_word[kMaxDevices] = {};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool supported_d(int d) { return d == 64 || d == 128 || d == 256; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+fa_status validate_common(int B, int H, int N, int d, float scale, int causal) {
+  if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return FA_ERR_INVALID_ARG;
+  if (!supported_d(d)) return FA_ERR_UNSUPPORTED;
+  // B*H and B*H*N*d must fit the 32-bit grid/coordinate ranges the kernels use.
+  const long long bh = (long long)B * H;
+  if (bh > 0x7fffffffLL || (long long)N > 0x7fffffffLL / 2) return FA_ERR_INVALID_ARG;
+  return FA_OK;
+}
+
+}  // namespace
+
+int* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_err_word[dev]) {
+    int* w = nullptr;
+    if (cudaMalloc(&w, 2 * sizeof(int)) != cudaSuccess) return nullptr;
+    if (cudaMemset(w, 0, 2 * sizeof(int)) != cudaSuccess) {
+      cudaFree(w);
+      return nullptr;
+    }
+    g_err_word[dev] = w;
+  }
+  return g_err_word[dev];
+}
+
+fa_status record_cuda_error(cudaError_t e) {
+  g_last_cuda_error = (int)e;
+  return FA_ERR_LAUNCH;
+}
+
+fa_status make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                        int elem_bytes, int inner, int N, int BH, int box_inner, int box_rows,
+                        CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return record_cuda_error(cudaErrorNotSupported);
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)inner * elem_bytes, (cuuint64_t)N * inner * elem_bytes};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return record_cuda_error(cudaErrorInvalidValue);
+  return FA_OK;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                 int N, int d, float scale, int causal, void* stream) {
+  fa_status s = validate_common(B, H, N, d, scale, causal);
+  if (s != FA_OK) return s;
+  if ((long long)B * H * N == 0) return FA_OK;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  return run_fwd(q, k, v, o, lse, B * H, N, d, scale, causal, (cudaStream_t)stream);
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d, int variant) {
+  if (B < 0 || H < 0 || N < 0 || !supported_d(d)) return 0;
+  if (variant != FA_BWD_AUTO && variant != FA_BWD_5GEMM && variant != FA_BWD_7GEMM) return 0;
+  const size_t bh = (size_t)B * H;
+  const size_t npad = round_up((size_t)N, 128);
+  size_t bytes = round_up(4 * bh * npad, 256);
+  if (variant != FA_BWD_7GEMM && bwd_supported(d, FA_BWD_5GEMM)) bytes += 4 * bh * npad * d;
+  return bytes + 256;
+}
+
+int fa_bwd_choose(int B, int H, int N, int d, int causal) {
+  (void)B;
+  (void)H;
+  (void)N;
+  (void)causal;
+  if (!bwd_supported(d, FA_BWD_5GEMM)) return FA_BWD_7GEMM;
+  return FA_BWD_7GEMM;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                 const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d,
+                 float scale, int causal, int variant, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+  fa_status s = validate_common(B, H, N, d, scale, causal);
+  if (s != FA_OK) return s;
+  if (variant != FA_BWD_AUTO && variant != FA_BWD_5GEMM && variant != FA_BWD_7GEMM)
+    return FA_ERR_INVALID_ARG;
+  if ((long long)B * H * N == 0) return FA_OK;
+  if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dO) ||
+      !aligned16(lse) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+    return FA_ERR_MISALIGNED;
+  const int chosen = variant == FA_BWD_AUTO ? fa_bwd_choose(B, H, N, d, causal) : variant;
+  if (!bwd_supported(d, chosen)) return FA_ERR_UNSUPPORTED;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+      workspace_bytes < fa_bwd_workspace_size(B, H, N, d, chosen))
+    return FA_ERR_WORKSPACE;
+  return run_bwd(q, k, v, o, dO, lse, dq, dk, dv, B * H, N, d, scale, causal, chosen, workspace,
+                 (cudaStream_t)stream);
+}
+
+fa_status fa_get_device_error(void* stream, int* site) {
+  if (site) *site = 0;
+  cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+  if (e != cudaSuccess) return record_cuda_error(e);
+  int* w = device_error_word();
+  if (!w) return record_cuda_error(cudaErrorMemoryAllocation);
+  int h[2] = {0, 0};
+  e = cudaMemcpy(h, w, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return record_cuda_error(e);
+  if (h[0] != 0) {
+    if (site) *site = h[1];
+    cudaMemset(w, 0, sizeof(h));
+    return FA_ERR_DEVICE_TIMEOUT;
+  }
+  return FA_OK;
+}
+
+int fa_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* fa_strerror(fa_status s) {
+  switch (s) {
+    case FA_OK: return "ok";
+    case FA_ERR_INVALID_ARG: return "invalid argument";
+    case FA_ERR_UNSUPPORTED: return "unsupported head dimension or variant";
+    case FA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case FA_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case FA_ERR_LAUNCH: return "CUDA launch failed";
+    case FA_ERR_DEVICE_TIMEOUT: return "in-kernel wait timed out";
+  }
+  return "unknown status";
+}
+
+int fa_fwd_launches(int B, int H, int N, int d) {
+  if ((long long)B * H * N <= 0 || !supported_d(d)) return 0;
+  return fwd_launch_count(d);
+}
+
+int fa_bwd_launches(int B, int H, int N, int d, int variant, int causal) {
+  if ((long long)B * H * N <= 0 || !supported_d(d)) return 0;
+  const int v = variant == FA_BWD_AUTO ? fa_bwd_choose(B, H, N, d, causal) : variant;
+  if (!bwd_supported(d, v)) return 0;
+  return bwd_launch_count(d, v);
+}
+
+}  // extern "C"

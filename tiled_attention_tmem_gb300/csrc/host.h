@@ -1,0 +1,48 @@
+// Host-side helpers shared by the launcher translation units (not part of the ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "fa.h"
+
+namespace fa {
+
+// Device error word (two ints) of the current device, created on first use.
+// Returns nullptr if it could not be created.
+int* device_error_word();
+
+// Records a CUDA runtime error code for fa_last_cuda_error and returns FA_ERR_LAUNCH.
+fa_status record_cuda_error(cudaError_t e);
+
+// Builds a 3-D TMA descriptor over a contiguous [BH, N, inner] tensor:
+// dims {inner, N, BH}, box {64, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
+fa_status make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,
+                        int elem_bytes, int inner, int N, int BH, int box_inner, int box_rows,
+                        CUtensorMapSwizzle swizzle);
+
+// Kernel launch helper: sets the dynamic shared memory limit and launches.
+template <class Kernel, class Params>
+fa_status launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                 const Params& p) {
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return record_cuda_error(e);
+  kernel<<<grid, block, smem, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda_error(e);
+  return FA_OK;
+}
+
+// Forward launcher (fwd.cu).  Arguments already validated.
+fa_status run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
+                  int d, float scale, int causal, cudaStream_t st);
+int fwd_launch_count(int d);
+
+// Backward launchers (bwd.cu).  Arguments already validated; workspace sized.
+fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                  const float* lse, void* dq, void* dk, void* dv, int BH, int N, int d,
+                  float scale, int causal, int variant, void* workspace, cudaStream_t st);
+bool bwd_supported(int d, int variant);
+int bwd_launch_count(int d, int variant);
+
+}  // namespace fa
