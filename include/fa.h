@@ -76,6 +76,7 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
 /*
  * Bytes of device workspace fa_bwd needs for this shape and variant
  * (FA_BWD_AUTO: the largest over the variants).  0 for invalid shapes.
+ *   log2-domain LSE per row:           4*B*H*Npad bytes
  *   D (fp32 row dot products dO.O):    4*B*H*Npad bytes
  *   5-GEMM only, fp32 dQ accumulator:  4*B*H*Npad*d bytes
  * with Npad = N rounded up to a multiple of 128, plus 256 bytes of alignment.

@@ -83,7 +83,13 @@ def test_bwd_validation(lib):
     if b.lib().fa_bwd_launches(1, 2, 128, 64, b.FA_BWD_7GEMM, 0) > 0:
         assert call(workspace=0) == b.FA_ERR_WORKSPACE
         assert call(workspace=A + 16) == b.FA_ERR_WORKSPACE
-        assert call(wsb=ws - 1 - 256 * 0 - 300) == b.FA_ERR_WORKSPACE
+        ws7 = b.fa_bwd_workspace_size(1, 2, 128, 64, b.FA_BWD_7GEMM)
+        assert call(wsb=ws7 - 16) == b.FA_ERR_WORKSPACE
+        ws5 = b.fa_bwd_workspace_size(1, 2, 128, 64, b.FA_BWD_5GEMM)
+        assert call(variant=b.FA_BWD_5GEMM, wsb=ws5 - 16) == b.FA_ERR_WORKSPACE
+        # head dim 256 has no 5-GEMM kernel
+        assert b.fa_bwd(A, A, A, A, A, A, A, A, A, 1, 2, 128, 256, 0.0625, 0, b.FA_BWD_5GEMM,
+                        A, ws5, None) == b.FA_ERR_UNSUPPORTED
 
 
 def test_workspace_sizes(lib):

@@ -1,0 +1,812 @@
+// Fused attention backward.
+//
+// Method: the backward recomputes P from the per-row log-sum-exp kept by the
+// forward instead of storing it ("ELI5: FlashAttention", recomputation), forms
+// D_i = dO_i . O_i, and then
+//   dV = P^T dO,  dP = dO V^T,  dS = P o (dP - D),  dK = scale dS^T Q,  dQ = scale dS K.
+// Two variants, as debated in "Potential algorithmic improvements for backward
+// pass" (FlashAttention issue 1172):
+//   5-GEMM: one kernel per K/V tile runs S, dP, dV, dK and dQ; each K/V tile's
+//           dQ contribution is added into an fp32 accumulator in global memory
+//           (bulk asynchronous reductions), then converted to bf16.
+//   7-GEMM: the dK/dV kernel runs S, dP, dV, dK; a second kernel walks each
+//           query tile over the K/V tiles like the forward and runs S, dP, dQ.
+//           No atomics, so the result is bitwise reproducible.
+//
+// Workspace (fp32, rows padded to Npad = 128 * ceil(N / 128) per head):
+//   lse2[bh][Npad]  LSE * log2(e) for valid rows, +inf for padding rows
+//   dd[bh][Npad]    D for valid rows, 0 for padding rows
+//   dqacc[bh][Npad][d] (5-GEMM) with the 16-byte chunks of row i permuted by
+//                   chunk ^ (i % 8), which makes the staging writes of both
+//                   dQ orientations free of shared-memory bank conflicts.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace fa {
+
+__device__ __forceinline__ int dq_swz(int i, int c) { return ((((c >> 2) ^ (i & 7))) << 2) | (c & 3); }
+
+__device__ __forceinline__ void wait_drain_bwd(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_test(bar, parity)) {
+    if (clock64() - t0 > kWaitLimitCycles) return;
+  }
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// ----------------------------------------------------------------- preprocess
+// One group of G = d/8 threads per row: D_i = sum_c dO_ic O_ic (fp32), the
+// log2-domain LSE, and (5-GEMM) zeroing of the row's fp32 dQ accumulator.
+struct PreParams {
+  const uint16_t* o;
+  const uint16_t* dO;
+  const float* lse;
+  float* lse2;
+  float* dd;
+  float* dqacc;  // nullptr for the 7-GEMM variant
+  int N, Npad, BH, d;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
+  constexpr int G = D / 8;
+  const long long rows = (long long)p.BH * p.Npad;
+  const int sub = threadIdx.x % G;
+  for (long long row = ((long long)blockIdx.x * 256 + threadIdx.x) / G; row < rows;
+       row += (long long)gridDim.x * 256 / G) {
+    const int bh = (int)(row / p.Npad);
+    const int i = (int)(row % p.Npad);
+    float acc = 0.f;
+    if (i < p.N) {
+      const size_t off = ((size_t)bh * p.N + i) * D + sub * 8;
+      const uint4 a = *reinterpret_cast<const uint4*>(p.o + off);
+      const uint4 b = *reinterpret_cast<const uint4*>(p.dO + off);
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), acc);
+        acc = fmaf(__uint_as_float(av[e] & 0xffff0000u), __uint_as_float(bv[e] & 0xffff0000u), acc);
+      }
+    }
+#pragma unroll
+    for (int w = G / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w, G);
+    if (sub == 0) {
+      p.dd[row] = acc;
+      p.lse2[row] = i < p.N ? p.lse[(size_t)bh * p.N + i] * kLog2e : INFINITY;
+    }
+    if (p.dqacc) {
+      float4* z = reinterpret_cast<float4*>(p.dqacc + (size_t)row * D + sub * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+}
+
+// --------------------------------------------------------------- dQ convert
+struct ConvParams {
+  const float* dqacc;
+  uint16_t* dq;
+  int N, Npad, BH;
+  float scale;
+};
+
+template <int D>
+__global__ void __launch_bounds__(256) bwd_conv_kernel(const ConvParams p) {
+  const long long n4 = (long long)p.BH * p.N * D / 4;  // groups of 4 output columns
+  for (long long g = (long long)blockIdx.x * 256 + threadIdx.x; g < n4; g += (long long)gridDim.x * 256) {
+    const long long e = g * 4;
+    const int c = (int)(e % D);
+    const long long rowg = e / D;  // bh * N + i
+    const int bh = (int)(rowg / p.N);
+    const int i = (int)(rowg % p.N);
+    const float4 v = *reinterpret_cast<const float4*>(p.dqacc + ((size_t)bh * p.Npad + i) * D + dq_swz(i, c));
+    uint2 out;
+    out.x = pack_bf16(v.x * p.scale, v.y * p.scale);
+    out.y = pack_bf16(v.z * p.scale, v.w * p.scale);
+    *reinterpret_cast<uint2*>(p.dq + e) = out;
+  }
+}
+
+// ------------------------------------------------------------ dK/dV kernel
+// CTA = one tile of 128 keys (the MMA M dimension for S^T, dP^T, dV, dK) of one
+// head, walking the query tiles of BM rows that can see it.  With DSPLIT = 2
+// each of two CTAs keeps half of the d columns of dV and dK (head dim 256).
+//
+//   S^T  = K Q^T     (A = K K-major, B = Q K-major)          -> TMEM fp32
+//   dP^T = V dO^T    (A = V K-major, B = dO K-major)          -> TMEM fp32
+//   P^T  = exp2(S^T*c - lse2), dS^T = P^T o (dP^T - D)       (thread = key row)
+//   dV  += P^T dO    (A = P^T from TMEM, B = dO MN-major)
+//   dK  += dS^T Q    (A = dS^T from TMEM, B = Q MN-major)
+//   5-GEMM, d = 128: dQ^T = K^T dS^T (A = K MN-major, B = dS^T smem MN-major),
+//                    lanes = d;  d = 64: dQ = dS K (A = dS^T smem MN-major,
+//                    B = K MN-major), lanes = query.  Drained by warps 8..11
+//                    through shared memory into bulk fp32 reductions.
+//
+// SEP: P^T and dS^T get their own TMEM columns, so S^T(i+1) and dP^T(i+1) are
+// issued before dV(i), dK(i), dQ(i) and overlap the softmax of tile i+1.
+// Otherwise they alias the S^T / dP^T columns and the MMA order is sequential.
+struct BwdKVParams {
+  CUtensorMap q_map;   // box {64, BM, 1}
+  CUtensorMap k_map;   // box {64, 128, 1}
+  CUtensorMap v_map;   // box {64, 128, 1}
+  CUtensorMap do_map;  // box {64, BM, 1}
+  const float* lse2;
+  const float* dd;
+  float* dqacc;
+  uint16_t* dk;
+  uint16_t* dv;
+  int* err;
+  int N, Npad, BH;
+  float scale_log2;
+  float scale;
+  int causal;
+};
+
+template <int D_, int BM_, bool DQ_, int DSPLIT_, int QS_, bool SEP_>
+struct BwdKVCfg {
+  static constexpr int D = D_, BM = BM_, DSPLIT = DSPLIT_, QS = QS_;
+  static constexpr bool DQ = DQ_, SEP = SEP_;
+  static constexpr bool DQ_T = DQ && D == 128;  // dQ^T (lanes = d) vs dQ (lanes = query)
+  static constexpr int BN = 128;
+  static constexpr int DH = D / DSPLIT;
+  static constexpr int PANELS = D / 64;
+  static constexpr uint32_t KV_PANEL = BN * 128;
+  static constexpr uint32_t KV_TILE = PANELS * KV_PANEL;
+  static constexpr uint32_t QD_PANEL = BM * 128;
+  static constexpr uint32_t QD_TILE = PANELS * QD_PANEL;
+  static constexpr uint32_t DS_PANEL = BN * 128;  // dS^T smem [128 keys][BM queries]
+  static constexpr uint32_t DS_TILE = (BM / 64) * DS_PANEL;
+  static constexpr uint32_t STAGE_TX = 2 * QD_TILE + 2 * BM * 4;  // bytes landing per stage
+  static constexpr uint32_t STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + KV_TILE;
+  static constexpr uint32_t OFF_STAGE = OFF_V + KV_TILE;  // Q, dO, lse2, dd per stage
+  static constexpr uint32_t OFF_DS = OFF_STAGE + QS * STAGE_BYTES;
+  static constexpr uint32_t OFF_STG = OFF_DS + (DQ ? DS_TILE : 0);
+  static constexpr uint32_t STG_BYTES = DQ ? BM * D * 4 : 0;
+  static constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;
+  static constexpr int B_KV = 0, B_QDFULL = 1, B_QDEMPTY = 1 + QS, B_SDP = 1 + 2 * QS,
+                       B_PDS = B_SDP + 1, B_MMA = B_PDS + 1, B_DQFULL = B_MMA + 1,
+                       B_DQFREE = B_DQFULL + 1, B_STGFREE = B_DQFREE + 1, B_STGFULL = B_STGFREE + 1,
+                       B_DONE = B_STGFULL + 1, NBAR = B_DONE + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+  // TMEM columns
+  static constexpr int T_ST = 0, T_DPT = BM;
+  static constexpr int T_PT = SEP ? 2 * BM : T_ST;
+  static constexpr int T_DST = SEP ? 2 * BM + BM / 2 : T_DPT;
+  static constexpr int T_ACC = SEP ? 3 * BM : 2 * BM;
+  static constexpr int T_DV = T_ACC, T_DK = T_ACC + DH, T_DQ = T_ACC + 2 * DH;
+  static constexpr int DQ_COLS = DQ ? (DQ_T ? BM : D) : 0;
+  static constexpr int TMEM_USED = T_DQ + DQ_COLS;
+  static constexpr uint32_t TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+  static constexpr int THREADS = DQ ? 384 : 256;
+  static_assert(TMEM_USED <= 512, "TMEM budget");
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(!SEP || QS >= 2, "overlapped order needs two query stages");
+  static_assert(!DQ || DSPLIT == 1, "5-GEMM keeps all of dQ's columns");
+  static_assert(!DQ || D == 64 ? true : (D == 128 && BM == 64), "dQ^T path needs M = d = 128");
+  static_assert(!(DQ && D == 64) || BM == 128, "dQ path needs M = BM = 128");
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_constant__ BwdKVParams p) {
+  constexpr int D = C::D, BM = C::BM, QS = C::QS, DH = C::DH;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw_addr);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
+  const int warp = warp_id();
+  const int lane = lane_id();
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+
+  if (threadIdx.x == 0) {
+    *abort_flag = (*reinterpret_cast<volatile int*>(p.err) != 0) ? 1 : 0;
+    mbar_init(BAR(C::B_KV), 1);
+    for (int s = 0; s < QS; ++s) {
+      mbar_init(BAR(C::B_QDFULL + s), 1);
+      mbar_init(BAR(C::B_QDEMPTY + s), 1);
+    }
+    mbar_init(BAR(C::B_SDP), 1);
+    mbar_init(BAR(C::B_PDS), 4);
+    mbar_init(BAR(C::B_MMA), 1);
+    mbar_init(BAR(C::B_DQFULL), 1);
+    mbar_init(BAR(C::B_DQFREE), 4);
+    mbar_init(BAR(C::B_STGFREE), 1);
+    mbar_init(BAR(C::B_STGFULL), 4);
+    mbar_init(BAR(C::B_DONE), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const CtaAbort ab{abort_flag, p.err};
+
+  // Tile coordinates: key tile kb (natural order: under the causal mask the
+  // first key tiles see the most query tiles and start first), head bh, d part h.
+  const int per_kb = p.BH * C::DSPLIT;
+  const int kb = blockIdx.x / per_kb;
+  const int bh = (blockIdx.x % per_kb) / C::DSPLIT;
+  const int h = blockIdx.x % C::DSPLIT;
+  const int k0 = kb * C::BN;
+  const int n_qt = (p.N + BM - 1) / BM;
+  const int qt0 = p.causal ? k0 / BM : 0;
+  const int n = n_qt - qt0;
+  const float* lse2_g = p.lse2 + (size_t)bh * p.Npad;
+  const float* dd_g = p.dd + (size_t)bh * p.Npad;
+
+  auto stage_q = [&](int s) { return sbase + C::OFF_STAGE + s * C::STAGE_BYTES; };
+  auto stage_do = [&](int s) { return stage_q(s) + C::QD_TILE; };
+  auto stage_lse = [&](int s) { return stage_q(s) + 2 * C::QD_TILE; };
+  auto stage_dd = [&](int s) { return stage_lse(s) + BM * 4; };
+
+  if (!*abort_flag) {
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        tma_prefetch_desc(&p.q_map);
+        tma_prefetch_desc(&p.k_map);
+        tma_prefetch_desc(&p.v_map);
+        tma_prefetch_desc(&p.do_map);
+        mbar_expect_tx(BAR(C::B_KV), 2 * C::KV_TILE);
+        for (int pn = 0; pn < C::PANELS; ++pn) {
+          tma_load_3d(sbase + C::OFF_K + pn * C::KV_PANEL, &p.k_map, BAR(C::B_KV), 64 * pn, k0, bh);
+          tma_load_3d(sbase + C::OFF_V + pn * C::KV_PANEL, &p.v_map, BAR(C::B_KV), 64 * pn, k0, bh);
+        }
+        int it = 0;
+        for (; it < n; ++it) {
+          const int s = it % QS;
+          if (!wait_one(BAR(C::B_QDEMPTY + s), ((it / QS) & 1) ^ 1, ab, (kKBwdKV << 8) | 1)) break;
+          const int qrow = (qt0 + it) * BM;
+          mbar_expect_tx(BAR(C::B_QDFULL + s), C::STAGE_TX);
+          for (int pn = 0; pn < C::PANELS; ++pn) {
+            tma_load_3d(stage_q(s) + pn * C::QD_PANEL, &p.q_map, BAR(C::B_QDFULL + s), 64 * pn, qrow, bh);
+            tma_load_3d(stage_do(s) + pn * C::QD_PANEL, &p.do_map, BAR(C::B_QDFULL + s), 64 * pn, qrow, bh);
+          }
+          bulk_load(stage_lse(s), lse2_g + qrow, BM * 4, BAR(C::B_QDFULL + s));
+          bulk_load(stage_dd(s), dd_g + qrow, BM * 4, BAR(C::B_QDFULL + s));
+        }
+        wait_drain_bwd(BAR(C::B_KV), 0);
+        for (int i = max(0, it - QS); i < it; ++i) wait_drain_bwd(BAR(C::B_QDFULL + i % QS), (i / QS) & 1);
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issue
+      if (lane == 0) {
+        constexpr uint32_t idS = make_idesc(128, BM, false, false);
+        constexpr uint32_t idAcc = make_idesc(128, DH, false, true);
+        const uint32_t kt = sbase + C::OFF_K, vt = sbase + C::OFF_V;
+        auto issue_sdp = [&](int s) {
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss(tmem + C::T_ST, desc_kmajor(kt, C::KV_PANEL, 16 * k),
+                   desc_kmajor(stage_q(s), C::QD_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss(tmem + C::T_DPT, desc_kmajor(vt, C::KV_PANEL, 16 * k),
+                   desc_kmajor(stage_do(s), C::QD_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+          mma_commit(BAR(C::B_SDP));
+        };
+        auto issue_acc = [&](int s, bool first) {
+          const uint32_t dob = stage_do(s) + h * (DH / 64) * C::QD_PANEL;
+          const uint32_t qb = stage_q(s) + h * (DH / 64) * C::QD_PANEL;
+#pragma unroll
+          for (int k = 0; k < BM / 16; ++k)
+            mma_ts(tmem + C::T_DV, tmem + C::T_PT + 8 * k, desc_mnmajor(dob, C::QD_PANEL, 16 * k), idAcc,
+                   (!first || k > 0) ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < BM / 16; ++k)
+            mma_ts(tmem + C::T_DK, tmem + C::T_DST + 8 * k, desc_mnmajor(qb, C::QD_PANEL, 16 * k), idAcc,
+                   (!first || k > 0) ? 1u : 0u);
+        };
+        auto issue_dq = [&]() {
+          const uint32_t ds = sbase + C::OFF_DS;
+          if constexpr (C::DQ_T) {
+            constexpr uint32_t id = make_idesc(128, BM, true, true);
+#pragma unroll
+            for (int k = 0; k < C::BN / 16; ++k)
+              mma_ss(tmem + C::T_DQ, desc_mnmajor(kt, C::KV_PANEL, 16 * k), desc_mnmajor(ds, C::DS_PANEL, 16 * k),
+                     id, k > 0 ? 1u : 0u);
+          } else {
+            constexpr uint32_t id = make_idesc(128, D, true, true);
+#pragma unroll
+            for (int k = 0; k < C::BN / 16; ++k)
+              mma_ss(tmem + C::T_DQ, desc_mnmajor(ds, C::DS_PANEL, 16 * k), desc_mnmajor(kt, C::KV_PANEL, 16 * k),
+                     id, k > 0 ? 1u : 0u);
+          }
+          mma_commit(BAR(C::B_DQFULL));
+        };
+        bool ok = wait_one(BAR(C::B_KV), 0, ab, (kKBwdKV << 8) | 2);
+        if (ok && n > 0) {
+          ok = wait_one(BAR(C::B_QDFULL + 0), 0, ab, (kKBwdKV << 8) | 3);
+          if (ok) {
+            tc_fence_after();
+            issue_sdp(0);
+          }
+        }
+        for (int i = 0; ok && i < n; ++i) {
+          const int s = i % QS;
+          if (!wait_one(BAR(C::B_PDS), i & 1, ab, (kKBwdKV << 8) | 4)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if constexpr (C::SEP) {
+            if (i + 1 < n) {
+              const int s1 = (i + 1) % QS;
+              if (!wait_one(BAR(C::B_QDFULL + s1), ((i + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_sdp(s1);
+            }
+          }
+          issue_acc(s, i == 0);
+          if constexpr (C::DQ) {
+            if (i > 0 && !wait_one(BAR(C::B_DQFREE), (i - 1) & 1, ab, (kKBwdKV << 8) | 6)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_dq();
+          }
+          mma_commit(BAR(C::B_MMA));
+          mma_commit(BAR(C::B_QDEMPTY + s));
+          if constexpr (!C::SEP) {
+            if (i + 1 < n) {
+              const int s1 = (i + 1) % QS;
+              if (!wait_one(BAR(C::B_QDFULL + s1), ((i + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_sdp(s1);
+            }
+          }
+        }
+        mma_commit(BAR(C::B_DONE));
+        wait_drain_bwd(BAR(C::B_DONE), 0);
+      }
+      __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
+      // ---------------------------------------------- P^T / dS^T (thread = key row)
+      const int quad = warp & 3;
+      const int r = quad * 32 + lane;
+      const int kj = k0 + r;
+      const bool key_ok = kj < p.N;
+      const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+      const float cs = p.scale_log2;
+      bool ok = true;
+      for (int i = 0; i < n; ++i) {
+        const int s = i % QS;
+        const int q0 = (qt0 + i) * BM;
+        if (!wait_warp(BAR(C::B_SDP), i & 1, ab, (kKBwdKV << 8) | 7) ||
+            !wait_warp(BAR(C::B_QDFULL + s), (i / QS) & 1, ab, (kKBwdKV << 8) | 8)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float* L = reinterpret_cast<const float*>(gbase + (stage_lse(s) - sbase));
+        const float* Dd = reinterpret_cast<const float*>(gbase + (stage_dd(s) - sbase));
+        const int lim = p.causal ? kj - q0 : -1;  // columns c < lim are masked (query < key)
+        uint8_t* ds_row = gbase + C::OFF_DS + r * 128;
+        // Writes one 32-column chunk of P^T and dS^T (packed bf16) to TMEM and,
+        // for the 5-GEMM variant, dS^T row r into the [128 keys][BM queries]
+        // swizzled shared-memory tile read by the dQ MMA.
+        auto store_chunk = [&](int c0, const uint32_t* pp, const uint32_t* pd) {
+          tmem_st_32x32b_x16(trow + C::T_PT + (c0 >> 1), pp);
+          tmem_st_32x32b_x16(trow + C::T_DST + (c0 >> 1), pd);
+          if constexpr (C::DQ) {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int ch = (c0 >> 3) + u;
+              const int pn = ch >> 3, cc = ch & 7;
+              *reinterpret_cast<uint4*>(ds_row + pn * C::DS_PANEL + ((cc ^ (r & 7)) << 4)) =
+                  make_uint4(pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
+            }
+          }
+        };
+        constexpr int HOLD = C::SEP ? BM / 2 : 16;
+        uint32_t pk_p[HOLD], pk_ds[HOLD];
+#pragma unroll
+        for (int c0 = 0; c0 < BM; c0 += 32) {
+          uint32_t sr[32], dr[32];
+          tmem_ld_32x32b_x32(trow + C::T_ST + c0, sr);
+          tmem_ld_32x32b_x32(trow + C::T_DPT + c0, dr);
+          tmem_wait_ld();
+          reg_fence<32>(sr);
+          reg_fence<32>(dr);
+          const int hb = C::SEP ? (c0 >> 1) : 0;
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float pv[2], dv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int c = c0 + e + u;
+              float pe = ex2(fmaf(__uint_as_float(sr[e + u]), cs, -L[c]));
+              if (!key_ok || c < lim) pe = 0.f;
+              pv[u] = pe;
+              dv[u] = pe * (__uint_as_float(dr[e + u]) - Dd[c]);
+            }
+            pk_p[hb + (e >> 1)] = pack_bf16(pv[0], pv[1]);
+            pk_ds[hb + (e >> 1)] = pack_bf16(dv[0], dv[1]);
+          }
+          if constexpr (!C::SEP) store_chunk(c0, pk_p, pk_ds);
+        }
+        if constexpr (C::SEP) {
+          // dV(i-1), dK(i-1), dQ(i-1) read P^T, dS^T (TMEM) and dS^T (smem): wait for them.
+          if (i > 0 && !wait_warp(BAR(C::B_MMA), (i - 1) & 1, ab, (kKBwdKV << 8) | 9)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int c0 = 0; c0 < BM; c0 += 32) store_chunk(c0, pk_p + (c0 >> 1), pk_ds + (c0 >> 1));
+        }
+        if constexpr (C::DQ) fence_proxy_async_smem();
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(C::B_PDS));
+      }
+      // ------------------------------------------------ dV, dK epilogue
+      if (ok && n > 0 && wait_warp(BAR(C::B_MMA), (n - 1) & 1, ab, (kKBwdKV << 8) | 10)) {
+        tc_fence_after();
+        const bool store = key_ok;
+        const size_t rowoff = ((size_t)bh * p.N + (size_t)(store ? kj : 0)) * D + h * DH;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          uint16_t* dst = (which == 0 ? p.dv : p.dk) + rowoff;
+          const float mul = which == 0 ? 1.f : p.scale;
+          const uint32_t tacc = trow + (which == 0 ? C::T_DV : C::T_DK);
+#pragma unroll
+          for (int c0 = 0; c0 < DH; c0 += 32) {
+            uint32_t rr[32];
+            tmem_ld_32x32b_x32(tacc + c0, rr);
+            tmem_wait_ld();
+            reg_fence<32>(rr);
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 2)
+              pk[e >> 1] = pack_bf16(__uint_as_float(rr[e]) * mul, __uint_as_float(rr[e + 1]) * mul);
+            if (store) {
+              uint4* o4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+          }
+        }
+      } else if (n == 0 && key_ok) {
+        // No query can see this key (possible only with ragged tails): zero gradients.
+        for (int c = 0; c < DH; c += 8) {
+          *reinterpret_cast<uint4*>(p.dv + ((size_t)bh * p.N + kj) * D + h * DH + c) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(p.dk + ((size_t)bh * p.N + kj) * D + h * DH + c) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    } else if (warp >= 8) {
+      if constexpr (C::DQ) {
+      // ------------------------------------------------------ dQ drain (5-GEMM)
+      const int quad = warp & 3;
+      const int lr = quad * 32 + lane;  // TMEM lane: d index (dQ^T) or query row (dQ)
+      const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16) + C::T_DQ;
+      float* stg = reinterpret_cast<float*>(gbase + C::OFF_STG);
+      const bool leader = (warp == 8 && lane == 0);
+      for (int i = 0; i < n; ++i) {
+        if (!wait_warp(BAR(C::B_DQFULL), i & 1, ab, (kKBwdKV << 8) | 11)) break;
+        tc_fence_after();
+        constexpr int COLS = C::DQ_COLS;
+        uint32_t v[COLS];
+#pragma unroll
+        for (int c0 = 0; c0 < COLS; c0 += 32) tmem_ld_32x32b_x32(trow + c0, v + c0);
+        tmem_wait_ld();
+        reg_fence<COLS>(v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(C::B_DQFREE));
+        // The previous bulk reduction must have finished reading the staging tile.
+        if (leader) {
+          bulk_wait_read0();
+          mbar_arrive(BAR(C::B_STGFREE));
+        }
+        if (!wait_warp(BAR(C::B_STGFREE), i & 1, ab, (kKBwdKV << 8) | 12)) break;
+        if constexpr (C::DQ_T) {
+          // lanes = d index lr, columns = query q of the tile
+#pragma unroll
+          for (int q = 0; q < COLS; ++q) stg[q * D + dq_swz(q, lr)] = __uint_as_float(v[q]);
+        } else {
+          // lanes = query row lr, columns = d
+#pragma unroll
+          for (int c = 0; c < COLS; c += 4)
+            *reinterpret_cast<float4*>(stg + lr * D + dq_swz(lr, c)) =
+                make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]), __uint_as_float(v[c + 2]),
+                            __uint_as_float(v[c + 3]));
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(C::B_STGFULL));
+        if (leader) {
+          if (!wait_one(BAR(C::B_STGFULL), i & 1, ab, (kKBwdKV << 8) | 13)) break;
+          const int q0 = (qt0 + i) * BM;
+          bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.Npad + q0) * D, smem_u32(stg), C::STG_BYTES);
+          bulk_commit();
+        }
+      }
+      if (leader) bulk_wait0();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------------- dQ kernel
+// 7-GEMM second kernel: CTA = 128 query rows of one head (M = query), walking
+// its K/V tiles in the same direction as the forward:
+//   S = Q K^T, dP = dO V^T (TMEM fp32), dS = P o (dP - D) (thread = query row)
+//   written back as bf16 over dP's columns, then dQ += dS K (A = dS from TMEM,
+//   B = K MN-major).  dQ * scale is written once at the end.
+struct BwdQParams {
+  CUtensorMap q_map;   // box {64, 128, 1}
+  CUtensorMap do_map;  // box {64, 128, 1}
+  CUtensorMap k_map;   // box {64, BN, 1}
+  CUtensorMap v_map;   // box {64, BN, 1}
+  const float* lse2;
+  const float* dd;
+  uint16_t* dq;
+  int* err;
+  int N, Npad, BH;
+  float scale_log2;
+  float scale;
+  int causal;
+};
+
+template <int D_, int BN_, int STAGES_>
+struct BwdQCfg {
+  static constexpr int D = D_, BN = BN_, STAGES = STAGES_;
+  static constexpr int PANELS = D / 64;
+  static constexpr uint32_t Q_PANEL = 128 * 128;
+  static constexpr uint32_t Q_TILE = PANELS * Q_PANEL;
+  static constexpr uint32_t KV_PANEL = BN * 128;
+  static constexpr uint32_t KV_TILE = PANELS * KV_PANEL;
+  static constexpr uint32_t OFF_Q = 0, OFF_DO = Q_TILE, OFF_KV = 2 * Q_TILE;
+  static constexpr uint32_t OFF_BAR = OFF_KV + STAGES * KV_TILE;
+  static constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES, B_SDP = 1 + 2 * STAGES,
+                       B_DS = B_SDP + 1, B_DQ = B_DS + 1, B_DONE = B_DQ + 1, NBAR = B_DONE + 1;
+  static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr int T_S = 0, T_DP = BN, T_DQ = 2 * BN;
+  static constexpr int TMEM_USED = 2 * BN + D;
+  static constexpr uint32_t TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
+  static constexpr int THREADS = 256;
+  static_assert(TMEM_USED <= 512 && SMEM_BYTES <= 232448, "budgets");
+};
+
+template <class C>
+__global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_constant__ BwdQParams p) {
+  constexpr int D = C::D, BN = C::BN, S = C::STAGES;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t sbase = (raw_addr + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (sbase - raw_addr);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
+  const int warp = warp_id();
+  const int lane = lane_id();
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+
+  if (threadIdx.x == 0) {
+    *abort_flag = (*reinterpret_cast<volatile int*>(p.err) != 0) ? 1 : 0;
+    mbar_init(BAR(C::B_QFULL), 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(BAR(C::B_KVFULL + s), 1);
+      mbar_init(BAR(C::B_KVEMPTY + s), 1);
+    }
+    mbar_init(BAR(C::B_SDP), 1);
+    mbar_init(BAR(C::B_DS), 4);
+    mbar_init(BAR(C::B_DQ), 1);
+    mbar_init(BAR(C::B_DONE), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+  const CtaAbort ab{abort_flag, p.err};
+
+  const int n_qt = (p.N + 127) / 128;
+  int qt = blockIdx.x / p.BH;
+  const int bh = blockIdx.x % p.BH;
+  if (p.causal) qt = n_qt - 1 - qt;
+  const int q0 = qt * 128;
+  int n;
+  {
+    const int last = p.causal ? min(q0 + 127, p.N - 1) : p.N - 1;
+    n = last / BN + 1;
+  }
+
+  if (!*abort_flag) {
+    if (warp == 0) {
+      if (lane == 0) {
+        tma_prefetch_desc(&p.q_map);
+        tma_prefetch_desc(&p.do_map);
+        tma_prefetch_desc(&p.k_map);
+        tma_prefetch_desc(&p.v_map);
+        mbar_expect_tx(BAR(C::B_QFULL), 2 * C::Q_TILE);
+        for (int pn = 0; pn < C::PANELS; ++pn) {
+          tma_load_3d(sbase + C::OFF_Q + pn * C::Q_PANEL, &p.q_map, BAR(C::B_QFULL), 64 * pn, q0, bh);
+          tma_load_3d(sbase + C::OFF_DO + pn * C::Q_PANEL, &p.do_map, BAR(C::B_QFULL), 64 * pn, q0, bh);
+        }
+        int it = 0;
+        bool ok = true;
+        for (int j = 0; j < n && ok; ++j) {
+          for (int w = 0; w < 2; ++w) {
+            const int s = it % S;
+            if (!wait_one(BAR(C::B_KVEMPTY + s), ((it / S) & 1) ^ 1, ab, (kKBwdQ << 8) | 1)) {
+              ok = false;
+              break;
+            }
+            mbar_expect_tx(BAR(C::B_KVFULL + s), C::KV_TILE);
+            const CUtensorMap* m = w ? &p.v_map : &p.k_map;
+            for (int pn = 0; pn < C::PANELS; ++pn)
+              tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m, BAR(C::B_KVFULL + s), 64 * pn,
+                          j * BN, bh);
+            ++it;
+          }
+        }
+        wait_drain_bwd(BAR(C::B_QFULL), 0);
+        for (int i = max(0, it - S); i < it; ++i) wait_drain_bwd(BAR(C::B_KVFULL + i % S), (i / S) & 1);
+      }
+      __syncwarp();
+    } else if (warp == 1) {
+      if (lane == 0) {
+        constexpr uint32_t idS = make_idesc(128, BN, false, false);
+        constexpr uint32_t idQ = make_idesc(128, D, false, true);
+        bool ok = wait_one(BAR(C::B_QFULL), 0, ab, (kKBwdQ << 8) | 2);
+        int it = 0;
+        for (int j = 0; ok && j < n; ++j) {
+          const int sk = it % S;
+          if (!wait_one(BAR(C::B_KVFULL + sk), (it / S) & 1, ab, (kKBwdQ << 8) | 3)) {
+            ok = false;
+            break;
+          }
+          ++it;
+          const int sv = it % S;
+          if (!wait_one(BAR(C::B_KVFULL + sv), (it / S) & 1, ab, (kKBwdQ << 8) | 3)) {
+            ok = false;
+            break;
+          }
+          ++it;
+          tc_fence_after();
+          const uint32_t kb = sbase + C::OFF_KV + sk * C::KV_TILE;
+          const uint32_t vb = sbase + C::OFF_KV + sv * C::KV_TILE;
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss(tmem + C::T_S, desc_kmajor(sbase + C::OFF_Q, C::Q_PANEL, 16 * k),
+                   desc_kmajor(kb, C::KV_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss(tmem + C::T_DP, desc_kmajor(sbase + C::OFF_DO, C::Q_PANEL, 16 * k),
+                   desc_kmajor(vb, C::KV_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+          mma_commit(BAR(C::B_SDP));
+          mma_commit(BAR(C::B_KVEMPTY + sv));
+          if (!wait_one(BAR(C::B_DS), j & 1, ab, (kKBwdQ << 8) | 4)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < BN / 16; ++k)
+            mma_ts(tmem + C::T_DQ, tmem + C::T_DP + 8 * k, desc_mnmajor(kb, C::KV_PANEL, 16 * k), idQ,
+                   (j > 0 || k > 0) ? 1u : 0u);
+          mma_commit(BAR(C::B_DQ));
+          mma_commit(BAR(C::B_KVEMPTY + sk));
+        }
+        mma_commit(BAR(C::B_DONE));
+        wait_drain_bwd(BAR(C::B_DONE), 0);
+      }
+      __syncwarp();
+    } else if (warp >= 4) {
+      const int quad = warp & 3;
+      const int r = quad * 32 + lane;
+      const int qi = q0 + r;
+      const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+      const float cs = p.scale_log2;
+      const float l2 = p.lse2[(size_t)bh * p.Npad + qi];  // +inf past N: every p is 0
+      const float dd = p.dd[(size_t)bh * p.Npad + qi];
+      const int limit = p.causal ? min(qi, p.N - 1) : p.N - 1;
+      bool ok = true;
+      for (int j = 0; j < n; ++j) {
+        if (!wait_warp(BAR(C::B_SDP), j & 1, ab, (kKBwdQ << 8) | 5)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int kbase = j * BN;
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          uint32_t sr[32], dr[32];
+          tmem_ld_32x32b_x32(trow + C::T_S + c0, sr);
+          tmem_ld_32x32b_x32(trow + C::T_DP + c0, dr);
+          tmem_wait_ld();
+          reg_fence<32>(sr);
+          reg_fence<32>(dr);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float dsv[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              float pe = ex2(fmaf(__uint_as_float(sr[e + u]), cs, -l2));
+              if (kbase + c0 + e + u > limit) pe = 0.f;
+              dsv[u] = pe * (__uint_as_float(dr[e + u]) - dd);
+            }
+            pk[e >> 1] = pack_bf16(dsv[0], dsv[1]);
+          }
+          // dS (bf16) over the first half of dP's columns: chunk c0 -> columns c0/2.
+          tmem_st_32x32b_x16(trow + C::T_DP + (c0 >> 1), pk);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(C::B_DS));
+      }
+      if (ok && wait_warp(BAR(C::B_DQ), (n - 1) & 1, ab, (kKBwdQ << 8) | 6)) {
+        tc_fence_after();
+        const bool store = qi < p.N;
+        uint16_t* dst = p.dq + ((size_t)bh * p.N + (size_t)(store ? qi : 0)) * D;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t rr[32];
+          tmem_ld_32x32b_x32(trow + C::T_DQ + c0, rr);
+          tmem_wait_ld();
+          reg_fence<32>(rr);
+          uint32_t pk[16];
+#pragma unroll
+          for (int e = 0; e < 32; e += 2)
+            pk[e >> 1] = pack_bf16(__uint_as_float(rr[e]) * p.scale, __uint_as_float(rr[e + 1]) * p.scale);
+          if (store) {
+            uint4* o4 = reinterpret_cast<uint4*>(dst + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace fa

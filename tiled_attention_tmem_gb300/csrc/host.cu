@@ -109,7 +109,7 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, int variant) {
   if (variant != FA_BWD_AUTO && variant != FA_BWD_5GEMM && variant != FA_BWD_7GEMM) return 0;
   const size_t bh = (size_t)B * H;
   const size_t npad = round_up((size_t)N, 128);
-  size_t bytes = round_up(4 * bh * npad, 256);
+  size_t bytes = 2 * round_up(4 * bh * npad, 256);  // log2-domain LSE and D per padded row
   if (variant != FA_BWD_7GEMM && bwd_supported(d, FA_BWD_5GEMM)) bytes += 4 * bh * npad * d;
   return bytes + 256;
 }
