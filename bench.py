@@ -1,0 +1,375 @@
+#!/usr/bin/env python
+"""Benchmark of the fused attention hot path on GB300.
+
+One step = the whole path once: fa_fwd (O, LSE) then fa_bwd (dQ, dK, dV) with the
+variant the library picks for the shape, on synthetic inputs drawn by
+``tiled_attention_tmem_gb300.inputs`` (i.i.d. normal, bf16).  Throughput counts
+nominal FLOPs: 4*B*H*N^2*d for the forward, 2.5x that for the backward, both
+halved under the causal mask.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Rank 0 prints one JSON line.  With N > 1 (launched by torch.distributed.run)
+every rank runs its own replica of the workload on its own GPU (the path has no
+cross-GPU exchange); the value is the total FLOPs of all ranks over the slowest
+rank's time.  ``--impl reference`` times the CPU fp64 oracle on a bounded sample
+of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS, bf16 d=128, and % of GB300 dense BF16 tensor peak"
+DEFAULT_WORKLOAD = "b4_h16_n2048_d128_causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM traffic per launch of the dominant kernel, read from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum).  Keyed by the workload and the
+# hash of the kernel sources it was taken on; any source change voids it.
+NCU_TRAFFIC = {}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--variant", choices=["auto", "5", "7"], default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def kernel_source_hash() -> str:
+    d = os.path.join(ROOT, "tiled_attention_tmem_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.lines: list[str] = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------- oracle timing
+
+
+def time_oracle(w, seconds: float, max_heads: int | None = None):
+    """Times the fp64 CPU oracle (forward + backward) on whole heads of the workload."""
+    import numpy as np
+
+    import oracle
+    from tiled_attention_tmem_gb300 import inputs as I
+    x = I.make_inputs(1, 1, w.N, w.d, seed=w.seed, sigma=w.sigma, k_shift=w.k_shift)
+    q, k, v, do = x.as_f64()
+    heads = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.forward(q, k, v, w.softmax_scale, w.causal)
+        oracle.backward(q, k, v, do, w.softmax_scale, w.causal)
+        heads += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_heads is not None and heads >= max_heads):
+            break
+    per_head = (w.fwd_flops + w.bwd_flops) / (w.B * w.H)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": per_head * heads / el / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{heads} whole head(s) of {w.name} (1 of B*H={w.B * w.H}), fp64 numpy with "
+                      f"multithreaded BLAS matmuls, forward + backward, {el:.1f} s",
+            "seconds": el}
+
+
+# -------------------------------------------------------------------- arms
+
+
+def run_reference(args, rank, world):
+    from tiled_attention_tmem_gb300 import inputs as I
+    w = I.WORKLOADS[args.workload]
+    if rank != 0:
+        return
+    per_head = (w.fwd_flops + w.bwd_flops) / (w.B * w.H)
+    # Each step is one whole head: a bounded sample of the workload.
+    for _ in range(args.warmup):
+        time_oracle(w, 0.0, max_heads=1)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle(w, 0.0, max_heads=1)
+    el = time.perf_counter() - t0
+    value = per_head * args.steps / el / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "step_sample": "one whole head (b=0, h=0) per step"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": "one whole head per step, fp64 numpy oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    from tiled_attention_tmem_gb300 import api, binding as b, build, inputs as I
+
+    build.build_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = I.WORKLOADS[args.workload]
+    variant = {"auto": b.FA_BWD_AUTO, "5": b.FA_BWD_5GEMM, "7": b.FA_BWD_7GEMM}[args.variant]
+    chosen = variant if variant != b.FA_BWD_AUTO else b.fa_bwd_choose(w.B, w.H, w.N, w.d, w.causal)
+
+    x = I.workload_inputs(w)
+    host = [torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+            for a in (x.q, x.k, x.v, x.do)]
+    q, k, v, do = (t.to(dev) for t in host)
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+    ws = torch.empty(b.fa_bwd_workspace_size(w.B, w.H, w.N, w.d, chosen), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > 129 MB L2
+    scale = w.softmax_scale
+    stream = torch.cuda.current_stream()
+
+    def step():
+        api.attention_forward(q, k, v, scale, w.causal, out=o, lse=lse)
+        api.attention_backward(q, k, v, o, do, lse, scale, w.causal, variant=chosen, workspace=ws,
+                               grads=grads)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    api.check_device_error()
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    b.fa_profile_start()
+    for i in range(args.steps):
+        flush.fill_(float(i))  # evict L2 between timed steps (outside the events)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    prof = b.fa_profile_stop()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    api.check_device_error()
+    times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_s = torch.tensor([sum(times_ms) / 1e3], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(total_s, op=dist.ReduceOp.MAX)
+    total_s = float(total_s.item())
+
+    flops_step = w.fwd_flops + w.bwd_flops
+    value = flops_step * args.steps * world / total_s / 1e12
+    launches = sum(n for n, _ in prof.values())
+
+    # Per-kernel timing from the library's own events (same stream as the kernels).
+    n_bh_flops = {
+        "fwd": w.fwd_flops,
+        "bwd_kv5": w.bwd_flops,           # S, dP, dV, dK, dQ: all five GEMMs
+        "bwd_kv7": w.bwd_flops * 4 / 5,   # S, dP, dV, dK
+        "bwd_q7": w.bwd_flops * 3 / 5,    # S, dP, dQ
+    }
+    kernels = {}
+    for name, (n, ms) in prof.items():
+        if n:
+            kernels[name] = {"launches": n, "ms_avg": ms / n, "share": None}
+    tot_ms = sum(v_["ms_avg"] * v_["launches"] for v_ in kernels.values())
+    for v_ in kernels.values():
+        v_["share"] = v_["ms_avg"] * v_["launches"] / tot_ms if tot_ms else None
+    dominant = max(kernels, key=lambda n_: kernels[n_]["ms_avg"] * kernels[n_]["launches"])
+    peaks, peak_src = load_peaks()
+    roof = None
+    if dominant in n_bh_flops:
+        ach = n_bh_flops[dominant] / (kernels[dominant]["ms_avg"] / 1e3) / 1e12
+        peak = float(peaks["bf16_tflops"])
+        tr = NCU_TRAFFIC.get((w.name, dominant, kernel_source_hash()))
+        roof = {"bound": "tensor", "kernel": dominant, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": tr,
+                "peak_source": f"bf16_tflops (burst) of {peak_src} peaks",
+                "frac_of_sustained": ach / float(peaks["bf16_tflops_sustained"])}
+    fwd_tf = w.fwd_flops / (kernels["fwd"]["ms_avg"] / 1e3) / 1e12 if "fwd" in kernels else None
+    bwd_ms = sum(kernels[n_]["ms_avg"] for n_ in ("bwd_pre", "bwd_kv5", "bwd_conv", "bwd_kv7", "bwd_q7")
+                 if n_ in kernels)
+    bwd_tf = w.bwd_flops / (bwd_ms / 1e3) / 1e12 if bwd_ms else None
+
+    # End to end through the public API: pinned host inputs in, gradients and
+    # forward outputs back to pinned host memory, every step.
+    out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, *grads)]
+    e2e_steps = max(1, min(args.e2e_steps, args.steps))
+
+    def e2e_step():
+        for hsrc, ddst in zip(host, (q, k, v, do)):
+            ddst.copy_(hsrc, non_blocking=True)
+        step()
+        for hdst, dsrc in zip(out_host, (o, lse, *grads)):
+            hdst.copy_(dsrc, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_e = []
+    for _ in range(e2e_steps):
+        s_, e_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s_.record(stream)
+        e2e_step()
+        e_.record(stream)
+        torch.cuda.synchronize()
+        t_e.append(s_.elapsed_time(e_))
+    e2e_s = torch.tensor([sum(t_e) / 1e3], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_s, op=dist.ReduceOp.MAX)
+    e2e_val = flops_step * e2e_steps * world / float(e2e_s.item()) / 1e12
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
+    api.check_device_error()
+
+    cpu = None
+    if rank == 0 and world == 1:
+        cpu = time_oracle(w, args.cpu_seconds)
+        cpu.pop("seconds", None)
+
+    if rank == 0:
+        frac = value / world / float(peaks["bf16_tflops"])
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": total_s / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                       "scale": scale, "bwd_variant": f"{chosen}-GEMM" + (" (auto)" if variant == 0 else ""),
+                       "l2": "flushed (256 MiB write) between timed steps, outside the timed events",
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
+            "frac_of_peak": frac, "peak_tflops": float(peaks["bf16_tflops"]),
+            "roofline": roof, "cpu_baseline": cpu,
+            "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": launches, "kernels": kernels, "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+        run_reference(args, rank, world)
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    run_ours(args, rank, world, local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

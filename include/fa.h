@@ -114,6 +114,33 @@ int fa_last_cuda_error(void);
 /* Static description of a status code. */
 const char* fa_strerror(fa_status s);
 
+/*
+ * Kernel-level timing for benchmarks (no counterpart in the method itself).
+ * Between fa_profile_start and fa_profile_stop the library records a pair of
+ * CUDA events around every kernel it launches, on that kernel's stream.
+ * fa_profile_stop synchronises on those events and fills, per kernel kind
+ * (FA_KERNEL_*), the number of launches and their summed device time in
+ * milliseconds.  Events are created by the library and reused; recording adds
+ * no device work beyond the event markers.  Not thread-safe against
+ * concurrent start/stop calls.
+ */
+enum {
+  FA_KERNEL_FWD = 0,      /* fused forward */
+  FA_KERNEL_BWD_PRE = 1,  /* D = rowsum(dO o O), log2-domain LSE, dQ accumulator zeroing */
+  FA_KERNEL_BWD_KV5 = 2,  /* 5-GEMM main kernel (dK, dV, fp32 dQ reductions) */
+  FA_KERNEL_BWD_CONV = 3, /* 5-GEMM dQ fp32 -> bf16 */
+  FA_KERNEL_BWD_KV7 = 4,  /* 7-GEMM dK/dV kernel */
+  FA_KERNEL_BWD_Q7 = 5,   /* 7-GEMM dQ kernel */
+  FA_KERNEL_KINDS = 6
+};
+typedef struct {
+  int launches[FA_KERNEL_KINDS];
+  double ms[FA_KERNEL_KINDS];
+} fa_profile;
+int fa_profile_start(void);
+int fa_profile_stop(fa_profile* out);
+const char* fa_kernel_name(int kind);
+
 /* Number of kernels one fa_fwd / fa_bwd call launches for this shape/variant. */
 int fa_fwd_launches(int B, int H, int N, int d);
 int fa_bwd_launches(int B, int H, int N, int d, int variant, int causal);

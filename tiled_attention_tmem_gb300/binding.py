@@ -40,6 +40,9 @@ SIGNATURES = {
     "fa_get_device_error": (_I, [_VP, ctypes.POINTER(_I)]),
     "fa_last_cuda_error": (_I, []),
     "fa_strerror": (ctypes.c_char_p, [_I]),
+    "fa_profile_start": (_I, []),
+    "fa_profile_stop": (_I, [_VP]),
+    "fa_kernel_name": (ctypes.c_char_p, [_I]),
     "fa_fwd_launches": (_I, [_I, _I, _I, _I]),
     "fa_bwd_launches": (_I, [_I, _I, _I, _I, _I, _I]),
 }
@@ -111,3 +114,24 @@ def fa_fwd_launches(B, H, N, d) -> int:
 
 def fa_bwd_launches(B, H, N, d, variant, causal=0) -> int:
     return lib().fa_bwd_launches(B, H, N, d, variant, int(causal))
+
+
+FA_KERNEL_KINDS = 6
+
+
+class FaProfile(ctypes.Structure):
+    _fields_ = [("launches", _I * FA_KERNEL_KINDS), ("ms", ctypes.c_double * FA_KERNEL_KINDS)]
+
+
+def fa_profile_start() -> int:
+    return lib().fa_profile_start()
+
+
+def fa_profile_stop() -> dict:
+    """Returns {kernel name: (launches, total ms)} for the kernels launched since start."""
+    prof = FaProfile()
+    st = lib().fa_profile_stop(ctypes.byref(prof))
+    if st != FA_OK:
+        raise FaError(st, "fa_profile_stop")
+    return {lib().fa_kernel_name(k).decode(): (prof.launches[k], prof.ms[k])
+            for k in range(FA_KERNEL_KINDS)}

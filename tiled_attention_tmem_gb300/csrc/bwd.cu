@@ -51,8 +51,10 @@ fa_status run_pre(const void* o, const void* dO, const float* lse, const Workspa
               N, Npad, BH, D};
   const long long threads = (long long)BH * Npad * (D / 8);
   const long long blocks = std::min<long long>((threads + 255) / 256, (long long)sm_count() * 8);
+  prof_before(FA_KERNEL_BWD_PRE, st);
   bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(p);
   cudaError_t e = cudaGetLastError();
+  prof_after(FA_KERNEL_BWD_PRE, st);
   return e == cudaSuccess ? FA_OK : record_cuda_error(e);
 }
 
@@ -61,8 +63,10 @@ fa_status run_conv(const Workspace& w, void* dq, int BH, int N, int Npad, float 
   ConvParams p{w.dqacc, static_cast<uint16_t*>(dq), N, Npad, BH, scale};
   const long long groups = (long long)BH * N * D / 4;
   const long long blocks = std::min<long long>((groups + 255) / 256, (long long)sm_count() * 8);
+  prof_before(FA_KERNEL_BWD_CONV, st);
   bwd_conv_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(p);
   cudaError_t e = cudaGetLastError();
+  prof_after(FA_KERNEL_BWD_CONV, st);
   return e == cudaSuccess ? FA_OK : record_cuda_error(e);
 }
 
@@ -92,7 +96,7 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
   p.causal = causal;
   const long long blocks = (long long)((N + C::BN - 1) / C::BN) * BH * C::DSPLIT;
   if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  return launch(bwd_kv_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  return launch(C::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);
 }
 
 template <class C>
@@ -119,7 +123,7 @@ fa_status run_q(const void* q, const void* k, const void* v, const void* dO, con
   p.causal = causal;
   const long long blocks = (long long)((N + 127) / 128) * BH;
   if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  return launch(bwd_q_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  return launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);
 }
 
 template <int D, class KV5, class KV7, class Q7>

@@ -38,7 +38,7 @@ fa_status run(const void* q, const void* k, const void* v, void* o, float* lse, 
   const int n_qblk = (N + 128 * C::NQ - 1) / (128 * C::NQ);
   const long long blocks = (long long)n_qblk * BH;
   if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  return launch(fwd_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  return launch(FA_KERNEL_FWD, fwd_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);
 }
 
 }  // namespace

@@ -20,15 +20,21 @@ fa_status make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType 
                         int elem_bytes, int inner, int N, int BH, int box_inner, int box_rows,
                         CUtensorMapSwizzle swizzle);
 
+// Profiling markers (no-ops unless fa_profile_start is active).
+void prof_before(int kind, cudaStream_t st);
+void prof_after(int kind, cudaStream_t st);
+
 // Kernel launch helper: sets the dynamic shared memory limit and launches.
 template <class Kernel, class Params>
-fa_status launch(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+fa_status launch(int kind, Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                  const Params& p) {
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return record_cuda_error(e);
+  prof_before(kind, st);
   kernel<<<grid, block, smem, st>>>(p);
   e = cudaGetLastError();
+  prof_after(kind, st);
   if (e != cudaSuccess) return record_cuda_error(e);
   return FA_OK;
 }
