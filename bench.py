@@ -38,7 +38,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM traffic per launch of the dominant kernel, read from one ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum).  Keyed by the workload and the
 # hash of the kernel sources it was taken on; any source change voids it.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("b4_h16_n2048_d128_causal", "bwd_kv5", "b74d458eb767cfb0"): 640.1e6,
+    ("b4_h16_n2048_d128_causal", "fwd", "b74d458eb767cfb0"): 148.2e6,
+}
 
 
 def parse_args():
@@ -282,7 +285,7 @@ def run_ours(args, rank, world, local_rank):
         peak = float(peaks["bf16_tflops"])
         tr = NCU_TRAFFIC.get((w.name, dominant, kernel_source_hash()))
         roof = {"bound": "tensor", "kernel": dominant, "achieved": ach, "peak": peak, "unit": "TFLOP/s",
-                "frac": ach / peak, "traffic": tr,
+                "frac": ach / peak, "traffic": tr, "traffic_unit": "bytes per launch (ncu dram read + write)",
                 "peak_source": f"bf16_tflops (burst) of {peak_src} peaks",
                 "frac_of_sustained": ach / float(peaks["bf16_tflops_sustained"])}
     fwd_tf = w.fwd_flops / (kernels["fwd"]["ms_avg"] / 1e3) / 1e12 if "fwd" in kernels else None
