@@ -96,6 +96,35 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int B, int H, int N, int d, float scale, int causal, int variant,
                  void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Backward that allocates nothing.  The pages have no counterpart to this: it
+ * exists for callers that cannot allocate device memory (code inside an
+ * allocator or memory-capped host, runtimes that only hand out input and
+ * output buffers).  Same arguments and results as fa_bwd, minus the workspace:
+ * the row statistics, the fp32 dQ accumulator and the in-kernel error word
+ * live in one static device array of FA_NOALLOC_SCRATCH_BYTES (+256) bytes
+ * that every GPU loading this library holds until the process exits.
+ *   - Scratch needed: 8*B*H*Npad bytes (7-GEMM) or 8*B*H*Npad + 4*B*H*Npad*d
+ *     (5-GEMM), Npad = N rounded up to 128.  FA_BWD_AUTO falls back to the
+ *     7-GEMM form when only that fits; a shape whose chosen variant does not
+ *     fit returns FA_ERR_WORKSPACE without launching anything.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.  Each
+ *     call clears the parts that must start at zero (error word, dQ
+ *     accumulator) itself.
+ *   - All calls share the array: calls that overlap on the GPU (other streams,
+ *     other host threads) race and must be serialised by the caller.
+ *   - An expired in-kernel wait is recorded in the array's error word, which
+ *     the next call clears; fa_get_device_error does not see it.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
+                         const float* lse, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, float scale, int causal, int variant,
+                         void* stream);
+
 /* The concrete variant (5 or 7) FA_BWD_AUTO runs for this shape. */
 int fa_bwd_choose(int B, int H, int N, int d, int causal);
 

@@ -36,6 +36,8 @@ SIGNATURES = {
     "fa_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                     _I, _I, _I, _I, _F, _I, _I, _VP, _SZ, _VP]),
+    "fa_bwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                            _I, _I, _I, _I, _F, _I, _I, _VP]),
     "fa_bwd_choose": (_I, [_I, _I, _I, _I, _I]),
     "fa_get_device_error": (_I, [_VP, ctypes.POINTER(_I)]),
     "fa_last_cuda_error": (_I, []),
@@ -92,6 +94,15 @@ def fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, variant,
            workspace, workspace_bytes, stream) -> int:
     return lib().fa_bwd(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, float(scale), int(causal),
                         variant, workspace, workspace_bytes, stream)
+
+
+def fa_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, variant, stream) -> int:
+    """The backward without a workspace: scratch lives in the library's static device array."""
+    return lib().fa_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, float(scale), int(causal),
+                                variant, stream)
+
+
+FA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def fa_bwd_choose(B, H, N, d, causal) -> int:
