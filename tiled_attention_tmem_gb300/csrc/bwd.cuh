@@ -154,6 +154,9 @@ template <int D_, int BM_, bool DQ_, int DSPLIT_, int QS_, bool SEP_>
 struct BwdKVCfg {
   static constexpr int D = D_, BM = BM_, DSPLIT = DSPLIT_, QS = QS_;
   static constexpr bool DQ = DQ_, SEP = SEP_;
+  // EARLY: the compute warps load all of S^T / dP^T into registers and release
+  // those TMEM columns at once, so S^T(i+1), dP^T(i+1) run during the softmax of i.
+  static constexpr bool EARLY = SEP && BM == 64;
   static constexpr bool DQ_T = DQ && D == 128;  // dQ^T (lanes = d) vs dQ (lanes = query)
   static constexpr int BN = 128;
   static constexpr int DH = D / DSPLIT;
@@ -176,7 +179,7 @@ struct BwdKVCfg {
   static constexpr int B_KV = 0, B_QDFULL = 1, B_QDEMPTY = 1 + QS, B_SDP = 1 + 2 * QS,
                        B_PDS = B_SDP + 1, B_MMA = B_PDS + 1, B_DQFULL = B_MMA + 1,
                        B_DQFREE = B_DQFULL + 1, B_STGFREE = B_DQFREE + 1, B_STGFULL = B_STGFREE + 1,
-                       B_DONE = B_STGFULL + 1, NBAR = B_DONE + 1;
+                       B_SCONS = B_STGFULL + 1, B_DONE = B_SCONS + 1, NBAR = B_DONE + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
   // TMEM columns
@@ -225,6 +228,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
     mbar_init(BAR(C::B_DQFREE), 4);
     mbar_init(BAR(C::B_STGFREE), 1);
     mbar_init(BAR(C::B_STGFULL), 4);
+    mbar_init(BAR(C::B_SCONS), 4);
     mbar_init(BAR(C::B_DONE), 1);
     fence_mbar_init();
   }
@@ -256,7 +260,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
   auto stage_lse = [&](int s) { return stage_q(s) + 2 * C::QD_TILE; };
   auto stage_dd = [&](int s) { return stage_lse(s) + BM * 4; };
 
+  // 5-GEMM (384 threads, 168 registers each at launch): each role branch
+  // starts with its warpgroup's register budget.  The producer/MMA warpgroup
+  // gives registers to the compute warpgroup; 128 * (80 + 224 + 168) stays
+  // within the 384 * 168 the block was launched with.
+  constexpr bool kSplitRegs = C::THREADS == 384;
   if (!*abort_flag) {
+    if (warp < 4) {
+    if constexpr (kSplitRegs) regs_shrink<80>();
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
@@ -342,12 +353,25 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         }
         for (int i = 0; ok && i < n; ++i) {
           const int s = i % QS;
+          if constexpr (C::EARLY) {
+            // S^T(i+1), dP^T(i+1) as soon as the compute warps hold S^T(i), dP^T(i) in registers.
+            if (i + 1 < n) {
+              const int s1 = (i + 1) % QS;
+              if (!wait_one(BAR(C::B_SCONS), i & 1, ab, (kKBwdKV << 8) | 14) ||
+                  !wait_one(BAR(C::B_QDFULL + s1), ((i + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_sdp(s1);
+            }
+          }
           if (!wait_one(BAR(C::B_PDS), i & 1, ab, (kKBwdKV << 8) | 4)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if constexpr (C::SEP) {
+          if constexpr (C::SEP && !C::EARLY) {
             if (i + 1 < n) {
               const int s1 = (i + 1) % QS;
               if (!wait_one(BAR(C::B_QDFULL + s1), ((i + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
@@ -385,8 +409,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         wait_drain_bwd(BAR(C::B_DONE), 0);
       }
       __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
+    }
+    } else if (warp < 8) {
       // ---------------------------------------------- P^T / dS^T (thread = key row)
+      if constexpr (kSplitRegs) regs_grow<224>();
       const int quad = warp & 3;
       const int r = quad * 32 + lane;
       const int kj = k0 + r;
@@ -425,30 +451,55 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         };
         constexpr int HOLD = C::SEP ? BM / 2 : 16;
         uint32_t pk_p[HOLD], pk_ds[HOLD];
+        // P^T = exp2(S^T c - lse2), dS^T = P^T (dP^T - D) for columns [c0, c0 + 32).
+        auto compute_chunk = [&](int c0, const uint32_t* sr, const uint32_t* dr, int hb) {
 #pragma unroll
-        for (int c0 = 0; c0 < BM; c0 += 32) {
-          uint32_t sr[32], dr[32];
-          tmem_ld_32x32b_x32(trow + C::T_ST + c0, sr);
-          tmem_ld_32x32b_x32(trow + C::T_DPT + c0, dr);
-          tmem_wait_ld();
-          reg_fence<32>(sr);
-          reg_fence<32>(dr);
-          const int hb = C::SEP ? (c0 >> 1) : 0;
+          for (int e = 0; e < 32; e += 4) {
+            const float4 l4 = *reinterpret_cast<const float4*>(L + c0 + e);
+            const float4 d4 = *reinterpret_cast<const float4*>(Dd + c0 + e);
+            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, ddv[4] = {d4.x, d4.y, d4.z, d4.w};
+            float pv[4], dv[4];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float pv[2], dv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
+            for (int u = 0; u < 4; ++u) {
               const int c = c0 + e + u;
-              float pe = ex2(fmaf(__uint_as_float(sr[e + u]), cs, -L[c]));
+              float pe = ex2(fmaf(__uint_as_float(sr[e + u]), cs, -lv[u]));
               if (!key_ok || c < lim) pe = 0.f;
               pv[u] = pe;
-              dv[u] = pe * (__uint_as_float(dr[e + u]) - Dd[c]);
+              dv[u] = pe * (__uint_as_float(dr[e + u]) - ddv[u]);
             }
             pk_p[hb + (e >> 1)] = pack_bf16(pv[0], pv[1]);
+            pk_p[hb + (e >> 1) + 1] = pack_bf16(pv[2], pv[3]);
             pk_ds[hb + (e >> 1)] = pack_bf16(dv[0], dv[1]);
+            pk_ds[hb + (e >> 1) + 1] = pack_bf16(dv[2], dv[3]);
           }
-          if constexpr (!C::SEP) store_chunk(c0, pk_p, pk_ds);
+        };
+        if constexpr (C::EARLY) {
+          uint32_t sr[BM], dr[BM];
+#pragma unroll
+          for (int c0 = 0; c0 < BM; c0 += 32) {
+            tmem_ld_32x32b_x32(trow + C::T_ST + c0, sr + c0);
+            tmem_ld_32x32b_x32(trow + C::T_DPT + c0, dr + c0);
+          }
+          tmem_wait_ld();
+          reg_fence<BM>(sr);
+          reg_fence<BM>(dr);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(C::B_SCONS));
+#pragma unroll
+          for (int c0 = 0; c0 < BM; c0 += 32) compute_chunk(c0, sr + c0, dr + c0, c0 >> 1);
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < BM; c0 += 32) {
+            uint32_t sr[32], dr[32];
+            tmem_ld_32x32b_x32(trow + C::T_ST + c0, sr);
+            tmem_ld_32x32b_x32(trow + C::T_DPT + c0, dr);
+            tmem_wait_ld();
+            reg_fence<32>(sr);
+            reg_fence<32>(dr);
+            compute_chunk(c0, sr, dr, C::SEP ? (c0 >> 1) : 0);
+            if constexpr (!C::SEP) store_chunk(c0, pk_p, pk_ds);
+          }
         }
         if constexpr (C::SEP) {
           // dV(i-1), dK(i-1), dQ(i-1) read P^T, dS^T (TMEM) and dS^T (smem): wait for them.

@@ -140,7 +140,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
   }
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
+  // Two softmax warpgroups (384 threads, 168 registers each at launch): the
+  // producer/MMA warpgroup gives registers to the softmax warpgroups;
+  // 128 * 80 + 256 * 208 stays within the 384 * 168 the block was launched with.
+  constexpr bool kSplitRegs = C::THREADS == 384;
   if (!*abort_flag) {
+    if (warp < 4) {
+    if constexpr (kSplitRegs) regs_shrink<80>();
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
@@ -247,8 +253,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
         wait_drain(BAR(C::B_DONE), 0);
       }
       __syncwarp();
-    } else if (warp >= 4) {
+    }
+    } else {
       // ------------------------------------------------------------ softmax
+      if constexpr (kSplitRegs) regs_grow<208>();
       const int t = (warp - 4) >> 2;
       const int quad = warp & 3;
       const int r = quad * 32 + lane;
