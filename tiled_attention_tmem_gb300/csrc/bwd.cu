@@ -10,7 +10,7 @@ namespace {
 
 // dK/dV kernel configurations <d, query rows per step, with dQ, d split, query stages, separate P/dS>.
 using KV5_64 = BwdKVCfg<64, 128, true, 1, 2, false>;
-using KV5_128 = BwdKVCfg<128, 64, true, 1, 3, true>;
+using KV5_128 = BwdKVCfg<128, 64, true, 1, 4, true>;
 using KV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
 using KV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
 using KV7_256 = BwdKVCfg<256, 64, false, 2, 1, false>;
@@ -94,6 +94,7 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
+  p.group = causal ? BH : head_group(((N + C::BN - 1) / C::BN) * C::DSPLIT, BH);
   const long long blocks = (long long)((N + C::BN - 1) / C::BN) * BH * C::DSPLIT;
   if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   return launch(C::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);
@@ -121,6 +122,7 @@ fa_status run_q(const void* q, const void* k, const void* v, const void* dO, con
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
+  p.group = causal ? BH : head_group((N + 127) / 128, BH);
   const long long blocks = (long long)((N + 127) / 128) * BH;
   if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   return launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);

@@ -148,6 +148,7 @@ struct BwdKVParams {
   float scale_log2;
   float scale;
   int causal;
+  int group;  // heads per launch-order group
 };
 
 template <int D_, int BM_, bool DQ_, int DSPLIT_, int QS_, bool SEP_>
@@ -174,7 +175,9 @@ struct BwdKVCfg {
   static constexpr uint32_t OFF_STAGE = OFF_V + KV_TILE;  // Q, dO, lse2, dd per stage
   static constexpr uint32_t OFF_DS = OFF_STAGE + QS * STAGE_BYTES;
   static constexpr uint32_t OFF_STG = OFF_DS + (DQ ? DS_TILE : 0);
-  static constexpr uint32_t STG_BYTES = DQ ? BM * D * 4 : 0;
+  // Shared-memory staging for bulk dQ reductions (dQ orientation only; dQ^T is
+  // reduced straight from registers).
+  static constexpr uint32_t STG_BYTES = (DQ && !DQ_T) ? BM * D * 4 : 0;
   static constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;
   static constexpr int B_KV = 0, B_QDFULL = 1, B_QDEMPTY = 1 + QS, B_SDP = 1 + 2 * QS,
                        B_PDS = B_SDP + 1, B_MMA = B_PDS + 1, B_DQFULL = B_MMA + 1,
@@ -244,10 +247,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
 
   // Tile coordinates: key tile kb (natural order: under the causal mask the
   // first key tiles see the most query tiles and start first), head bh, d part h.
-  const int per_kb = p.BH * C::DSPLIT;
-  const int kb = blockIdx.x / per_kb;
-  const int bh = (blockIdx.x % per_kb) / C::DSPLIT;
-  const int h = blockIdx.x % C::DSPLIT;
+  int tile, bh;
+  grouped_order(blockIdx.x, ((p.N + C::BN - 1) / C::BN) * C::DSPLIT, p.BH, p.group, tile, bh);
+  const int kb = tile / C::DSPLIT;
+  const int h = tile % C::DSPLIT;
   const int k0 = kb * C::BN;
   const int n_qt = (p.N + BM - 1) / BM;
   const int qt0 = p.causal ? k0 / BM : 0;
@@ -571,17 +574,21 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(C::B_DQFREE));
+        if constexpr (C::DQ_T) {
+          // lanes = d index lr, columns = query q of the tile: for each q the warp
+          // adds 32 consecutive floats of accumulator row q (one 128-byte line).
+          float* rows = p.dqacc + ((size_t)bh * p.Npad + (size_t)(qt0 + i) * BM) * D;
+#pragma unroll
+          for (int q = 0; q < COLS; ++q) red_add_f32(rows + q * D + dq_swz(q, lr), __uint_as_float(v[q]));
+          continue;
+        }
         // The previous bulk reduction must have finished reading the staging tile.
         if (leader) {
           bulk_wait_read0();
           mbar_arrive(BAR(C::B_STGFREE));
         }
         if (!wait_warp(BAR(C::B_STGFREE), i & 1, ab, (kKBwdKV << 8) | 12)) break;
-        if constexpr (C::DQ_T) {
-          // lanes = d index lr, columns = query q of the tile
-#pragma unroll
-          for (int q = 0; q < COLS; ++q) stg[q * D + dq_swz(q, lr)] = __uint_as_float(v[q]);
-        } else {
+        {
           // lanes = query row lr, columns = d
 #pragma unroll
           for (int c = 0; c < COLS; c += 4)
@@ -631,6 +638,7 @@ struct BwdQParams {
   float scale_log2;
   float scale;
   int causal;
+  int group;  // heads per launch-order group
 };
 
 template <int D_, int BN_, int STAGES_>
@@ -692,8 +700,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
   const CtaAbort ab{abort_flag, p.err};
 
   const int n_qt = (p.N + 127) / 128;
-  int qt = blockIdx.x / p.BH;
-  const int bh = blockIdx.x % p.BH;
+  int qt, bh;
+  grouped_order(blockIdx.x, n_qt, p.BH, p.group, qt, bh);
   if (p.causal) qt = n_qt - 1 - qt;
   const int q0 = qt * 128;
   int n;

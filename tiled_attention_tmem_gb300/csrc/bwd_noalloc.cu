@@ -103,6 +103,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   kp.scale_log2 = scale * kLog2e;
   kp.scale = scale;
   kp.causal = causal;
+  kp.group = causal ? BH : head_group(((N + KV::BN - 1) / KV::BN) * KV::DSPLIT, BH);
   const long long kv_blocks = (long long)((N + KV::BN - 1) / KV::BN) * BH * KV::DSPLIT;
   if ((s = launch(KV::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<KV>, dim3((unsigned)kv_blocks),
                   dim3(KV::THREADS), KV::SMEM_BYTES, st, kp)) != FA_OK)
@@ -130,6 +131,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   qp.scale_log2 = scale * kLog2e;
   qp.scale = scale;
   qp.causal = causal;
+  qp.group = causal ? BH : head_group((N + 127) / 128, BH);
   const long long q_blocks = (long long)((N + 127) / 128) * BH;
   return launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<Q7>, dim3((unsigned)q_blocks), dim3(Q7::THREADS), Q7::SMEM_BYTES,
                 st, qp);
@@ -137,7 +139,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
 
 // Same tile configurations as the workspace-taking backward.
 using NKV5_64 = BwdKVCfg<64, 128, true, 1, 2, false>;
-using NKV5_128 = BwdKVCfg<128, 64, true, 1, 3, true>;
+using NKV5_128 = BwdKVCfg<128, 64, true, 1, 4, true>;
 using NKV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
 using NKV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
 using NKV7_256 = BwdKVCfg<256, 64, false, 2, 1, false>;

@@ -52,6 +52,20 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const C
   return __all_sync(0xffffffffu, ok);
 }
 
+// Launch order with L2 locality.  Blocks are grouped by heads: a group holds
+// `group` consecutive heads and all of their `tiles` tiles, so the blocks that
+// share a head's K/V (forward) or Q/dO (backward) run at the same time and read
+// them from L2.  Inside a group, tile rank 0 (the heaviest under the causal
+// mask) comes first and the head varies fastest.
+__device__ __forceinline__ void grouped_order(int L, int tiles, int BH, int group, int& tile, int& bh) {
+  const int per_group = group * tiles;
+  const int g0 = (L / per_group) * group;
+  const int r = L % per_group;
+  const int gsize = min(group, BH - g0);
+  tile = r / gsize;
+  bh = g0 + r % gsize;
+}
+
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

@@ -36,6 +36,7 @@ fa_status run(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.scale_log2 = scale * kLog2e;
   p.causal = causal;
   const int n_qblk = (N + 128 * C::NQ - 1) / (128 * C::NQ);
+  p.group = causal ? BH : head_group(n_qblk, BH);
   const long long blocks = (long long)n_qblk * BH;
   if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   return launch(FA_KERNEL_FWD, fwd_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);

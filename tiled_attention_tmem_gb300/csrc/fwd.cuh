@@ -39,6 +39,7 @@ struct FwdParams {
   int BH;
   float scale_log2;  // scale * log2(e)
   int causal;
+  int group;  // heads per launch-order group
 };
 
 template <int D_, int NQ_, int BN_, int STAGES_>
@@ -125,10 +126,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
   const CtaAbort ab{abort_flag, p.err};
 
   // Tile coordinates: causal launches walk query blocks from the last (the most
-  // key tiles) to the first so the longest CTAs start first.
+  // key tiles) to the first so the longest CTAs of a head group start first.
   const int n_qblk = (p.N + 128 * NQ - 1) / (128 * NQ);
-  int qb = blockIdx.x / p.BH;
-  const int bh = blockIdx.x % p.BH;
+  int qb, bh;
+  grouped_order(blockIdx.x, n_qblk, p.BH, p.group, qb, bh);
   if (p.causal) qb = n_qblk - 1 - qb;
   const int q0 = qb * 128 * NQ;
   int nkv[NQ];

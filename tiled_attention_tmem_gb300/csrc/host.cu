@@ -67,6 +67,20 @@ int* device_error_word() {
   return g_err_word[dev];
 }
 
+int head_group(int tiles_per_head, int BH) {
+  static int sms[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    sms[dev] = n;
+  }
+  const int t = tiles_per_head > 0 ? tiles_per_head : 1;
+  const int g = (2 * sms[dev] + t - 1) / t;
+  return g < 1 ? 1 : (g > BH ? BH : g);
+}
+
 fa_status record_cuda_error(cudaError_t e) {
   g_last_cuda_error = (int)e;
   return FA_ERR_LAUNCH;

@@ -20,6 +20,12 @@ fa_status make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType 
                         int elem_bytes, int inner, int N, int BH, int box_inner, int box_rows,
                         CUtensorMapSwizzle swizzle);
 
+// Heads per launch-order group: enough heads for about two waves of blocks on
+// this device (at least 1, at most BH).  Launchers use one group of all heads
+// under the causal mask, where heaviest-tile-first across every head balances
+// better than locality helps.
+int head_group(int tiles_per_head, int BH);
+
 // Profiling markers (no-ops unless fa_profile_start is active).
 void prof_before(int kind, cudaStream_t st);
 void prof_after(int kind, cudaStream_t st);
