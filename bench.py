@@ -66,6 +66,19 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def aggregate_throughput(local_seconds: float, flops_per_step: float, steps: int, device=None) -> tuple[float, float]:
+    """Whole-job TFLOP/s of a replicated run: every rank ran `steps` steps of the same
+    workload; the job's time is the slowest rank's.  Returns (TFLOP/s, max seconds)."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    tmax = float(t.item())
+    return flops_per_step * steps * world / tmax / 1e12, tmax
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -254,13 +267,8 @@ def run_ours(args, rank, world, local_rank):
     clocks = sampler.stop()
     api.check_device_error()
     times_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_s = torch.tensor([sum(times_ms) / 1e3], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(total_s, op=dist.ReduceOp.MAX)
-    total_s = float(total_s.item())
-
     flops_step = w.fwd_flops + w.bwd_flops
-    value = flops_step * args.steps * world / total_s / 1e12
+    value, total_s = aggregate_throughput(sum(times_ms) / 1e3, flops_step, args.steps, dev)
     launches = sum(n for n, _ in prof.values())
 
     # Per-kernel timing from the library's own events (same stream as the kernels).
@@ -317,10 +325,7 @@ def run_ours(args, rank, world, local_rank):
         e_.record(stream)
         torch.cuda.synchronize()
         t_e.append(s_.elapsed_time(e_))
-    e2e_s = torch.tensor([sum(t_e) / 1e3], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(e2e_s, op=dist.ReduceOp.MAX)
-    e2e_val = flops_step * e2e_steps * world / float(e2e_s.item()) / 1e12
+    e2e_val, _ = aggregate_throughput(sum(t_e) / 1e3, flops_step, e2e_steps, dev)
     h2d = sum(t.numel() * t.element_size() for t in host)
     d2h = sum(t.numel() * t.element_size() for t in out_host)
     api.check_device_error()
