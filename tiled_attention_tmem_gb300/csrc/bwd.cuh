@@ -14,8 +14,10 @@
 //           No atomics, so the result is bitwise reproducible.
 //
 // Workspace (fp32, rows padded to Npad = 128 * ceil(N / 128) per head):
-//   lse2[bh][Npad]  LSE * log2(e) for valid rows, +inf for padding rows
-//   dd[bh][Npad]    D for valid rows, 0 for padding rows
+//   lse2[bh][Npad]  -LSE * log2(e) for valid rows, -inf for padding rows
+//   dd[bh][Npad]    -D for valid rows, 0 for padding rows
+//   (stored negated so P = exp2(S c + lse2) and dS = P (dP + dd) are single
+//   packed FMA / add instructions)
 //   dqacc[bh][Npad][d] (5-GEMM) with the 16-byte chunks of row i permuted by
 //                   chunk ^ (i % 8), which makes the staging writes of both
 //                   dQ orientations free of shared-memory bank conflicts.
@@ -44,7 +46,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 
 // ----------------------------------------------------------------- preprocess
 // One group of G = d/8 threads per row: D_i = sum_c dO_ic O_ic (fp32), the
-// log2-domain LSE, and (5-GEMM) zeroing of the row's fp32 dQ accumulator.
+// log2-domain LSE (both stored negated), and (5-GEMM) zeroing of the row's fp32
+// dQ accumulator.
 struct PreParams {
   const uint16_t* o;
   const uint16_t* dO;
@@ -79,8 +82,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
 #pragma unroll
     for (int w = G / 2; w > 0; w >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, w, G);
     if (sub == 0) {
-      p.dd[row] = acc;
-      p.lse2[row] = i < p.N ? p.lse[(size_t)bh * p.N + i] * kLog2e : INFINITY;
+      p.dd[row] = -acc;
+      p.lse2[row] = i < p.N ? -(p.lse[(size_t)bh * p.N + i] * kLog2e) : -INFINITY;
     }
     if (p.dqacc) {
       float4* z = reinterpret_cast<float4*>(p.dqacc + (size_t)row * D + sub * 8);
@@ -168,6 +171,7 @@ struct BwdKVCfg {
   static constexpr uint32_t QD_TILE = PANELS * QD_PANEL;
   static constexpr uint32_t DS_PANEL = BN * 128;  // dS^T smem [128 keys][BM queries]
   static constexpr uint32_t DS_TILE = (BM / 64) * DS_PANEL;
+  static constexpr int PREFETCH = QS + 2;  // query tiles ahead for L2 prefetch
   static constexpr uint32_t STAGE_TX = 2 * QD_TILE + 2 * BM * 4;  // bytes landing per stage
   static constexpr uint32_t STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
   static constexpr uint32_t OFF_K = 0;
@@ -295,6 +299,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           }
           bulk_load(stage_lse(s), lse2_g + qrow, BM * 4, BAR(C::B_QDFULL + s));
           bulk_load(stage_dd(s), dd_g + qrow, BM * 4, BAR(C::B_QDFULL + s));
+          // Stage loads can only start once a slot frees up (about two tiles ahead of
+          // use); pull the tiles further ahead into L2 so those loads hit L2.
+          if (it + C::PREFETCH < n) {
+            const int prow = (qt0 + it + C::PREFETCH) * BM;
+            for (int pn = 0; pn < C::PANELS; ++pn) {
+              tma_prefetch_l2_3d(&p.q_map, 64 * pn, prow, bh);
+              tma_prefetch_l2_3d(&p.do_map, 64 * pn, prow, bh);
+            }
+          }
         }
         wait_drain_bwd(BAR(C::B_KV), 0);
         for (int i = max(0, it - QS); i < it; ++i) wait_drain_bwd(BAR(C::B_QDFULL + i % QS), (i / QS) & 1);
@@ -455,25 +468,35 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         constexpr int HOLD = C::SEP ? BM / 2 : 16;
         uint32_t pk_p[HOLD], pk_ds[HOLD];
         // P^T = exp2(S^T c - lse2), dS^T = P^T (dP^T - D) for columns [c0, c0 + 32).
+        const float2 c2 = make_float2(cs, cs);
         auto compute_chunk = [&](int c0, const uint32_t* sr, const uint32_t* dr, int hb) {
+          // Masks only in chunks that reach past the last key or below the diagonal.
+          const bool masked = !key_ok || lim > c0;
 #pragma unroll
           for (int e = 0; e < 32; e += 4) {
             const float4 l4 = *reinterpret_cast<const float4*>(L + c0 + e);
             const float4 d4 = *reinterpret_cast<const float4*>(Dd + c0 + e);
-            const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, ddv[4] = {d4.x, d4.y, d4.z, d4.w};
-            float pv[4], dv[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int c = c0 + e + u;
-              float pe = ex2(fmaf(__uint_as_float(sr[e + u]), cs, -lv[u]));
-              if (!key_ok || c < lim) pe = 0.f;
-              pv[u] = pe;
-              dv[u] = pe * (__uint_as_float(dr[e + u]) - ddv[u]);
+            const float2 x01 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
+                                     make_float2(l4.x, l4.y));
+            const float2 x23 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2,
+                                     make_float2(l4.z, l4.w));
+            float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+            float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+            if (masked) {
+              const int c = c0 + e;
+              if (!key_ok || c < lim) p01.x = 0.f;
+              if (!key_ok || c + 1 < lim) p01.y = 0.f;
+              if (!key_ok || c + 2 < lim) p23.x = 0.f;
+              if (!key_ok || c + 3 < lim) p23.y = 0.f;
             }
-            pk_p[hb + (e >> 1)] = pack_bf16(pv[0], pv[1]);
-            pk_p[hb + (e >> 1) + 1] = pack_bf16(pv[2], pv[3]);
-            pk_ds[hb + (e >> 1)] = pack_bf16(dv[0], dv[1]);
-            pk_ds[hb + (e >> 1) + 1] = pack_bf16(dv[2], dv[3]);
+            const float2 d01 = fmul2(p01, fadd2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                                make_float2(d4.x, d4.y)));
+            const float2 d23 = fmul2(p23, fadd2(make_float2(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
+                                                make_float2(d4.z, d4.w)));
+            pk_p[hb + (e >> 1)] = pack_bf16(p01.x, p01.y);
+            pk_p[hb + (e >> 1) + 1] = pack_bf16(p23.x, p23.y);
+            pk_ds[hb + (e >> 1)] = pack_bf16(d01.x, d01.y);
+            pk_ds[hb + (e >> 1) + 1] = pack_bf16(d23.x, d23.y);
           }
         };
         if constexpr (C::EARLY) {
@@ -736,6 +759,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
             for (int pn = 0; pn < C::PANELS; ++pn)
               tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m, BAR(C::B_KVFULL + s), 64 * pn,
                           j * BN, bh);
+            if (j + 4 < n)
+              for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(m, 64 * pn, (j + 4) * BN, bh);
             ++it;
           }
         }
@@ -797,8 +822,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
       const int qi = q0 + r;
       const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
       const float cs = p.scale_log2;
-      const float l2 = p.lse2[(size_t)bh * p.Npad + qi];  // +inf past N: every p is 0
+      const float l2 = p.lse2[(size_t)bh * p.Npad + qi];  // -inf past N: every p is 0
       const float dd = p.dd[(size_t)bh * p.Npad + qi];
+      const float2 c2 = make_float2(cs, cs), l22 = make_float2(l2, l2), dd2 = make_float2(dd, dd);
       const int limit = p.causal ? min(qi, p.N - 1) : p.N - 1;
       bool ok = true;
       for (int j = 0; j < n; ++j) {
@@ -817,16 +843,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
           reg_fence<32>(sr);
           reg_fence<32>(dr);
           uint32_t pk[16];
+          const bool masked = kbase + c0 + 31 > limit;
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
-            float dsv[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-              float pe = ex2(fmaf(__uint_as_float(sr[e + u]), cs, -l2));
-              if (kbase + c0 + e + u > limit) pe = 0.f;
-              dsv[u] = pe * (__uint_as_float(dr[e + u]) - dd);
+            const float2 x = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, l22);
+            float2 pe = make_float2(ex2(x.x), ex2(x.y));
+            if (masked) {
+              if (kbase + c0 + e > limit) pe.x = 0.f;
+              if (kbase + c0 + e + 1 > limit) pe.y = 0.f;
             }
-            pk[e >> 1] = pack_bf16(dsv[0], dsv[1]);
+            const float2 ds =
+                fmul2(pe, fadd2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), dd2));
+            pk[e >> 1] = pack_bf16(ds.x, ds.y);
           }
           // dS (bf16) over the first half of dP's columns: chunk c0 -> columns c0/2.
           tmem_st_32x32b_x16(trow + C::T_DP + (c0 >> 1), pk);

@@ -46,6 +46,7 @@ template <int D_, int NQ_, int BN_, int STAGES_>
 struct FwdCfg {
   static constexpr int D = D_, NQ = NQ_, BN = BN_, STAGES = STAGES_;
   static constexpr int BM = 128;
+  static constexpr int PREFETCH = STAGES / 2 + 2;  // K/V tiles ahead for L2 prefetch
   static constexpr int PANELS = D / 64;
   static constexpr uint32_t Q_PANEL = BM * 128;
   static constexpr uint32_t Q_TILE = PANELS * Q_PANEL;
@@ -173,6 +174,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
             for (int pn = 0; pn < C::PANELS; ++pn)
               tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m,
                           BAR(C::B_KVFULL + s), 64 * pn, j * BN, bh);
+            // Pull K/V tiles a few steps beyond the ring into L2.
+            if (j + C::PREFETCH < nmax)
+              for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(m, 64 * pn, (j + C::PREFETCH) * BN, bh);
             ++it;
           }
         }
@@ -288,13 +292,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           for (int c = 0; c < BN; ++c)
             if (kbase + c > limit) sr[c] = __float_as_uint(-INFINITY);
         }
+        // Row maximum: four independent chains of three-input max.
         float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < BN; c += 4) {
-          mx0 = fmaxf(mx0, __uint_as_float(sr[c]));
-          mx1 = fmaxf(mx1, __uint_as_float(sr[c + 1]));
-          mx2 = fmaxf(mx2, __uint_as_float(sr[c + 2]));
-          mx3 = fmaxf(mx3, __uint_as_float(sr[c + 3]));
+        for (int c = 0; c < BN; c += 8) {
+          mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+          mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+          mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+          mx3 = max3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
         }
         const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs;
         const bool need = m_cand > m_used + 8.0f;
@@ -305,21 +310,27 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           l *= alpha;
         }
         const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-        float l0 = 0.f, l1 = 0.f;
+        // p = exp2(s * c - m), two columns per packed FMA / add.
+        const float2 c2 = make_float2(cs, cs), nm2 = make_float2(-msub, -msub);
+        float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < BN; c += 32) {
           uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[c + e]), cs, -msub));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[c + e + 1]), cs, -msub));
-            l0 += p0;
-            l1 += p1;
-            pk[e >> 1] = pack_bf16(p0, p1);
+          for (int e = 0; e < 32; e += 4) {
+            const float2 x01 = ffma2(make_float2(__uint_as_float(sr[c + e]), __uint_as_float(sr[c + e + 1])), c2, nm2);
+            const float2 x23 =
+                ffma2(make_float2(__uint_as_float(sr[c + e + 2]), __uint_as_float(sr[c + e + 3])), c2, nm2);
+            const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+            const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+            la = fadd2(la, p01);
+            lb = fadd2(lb, p23);
+            pk[e >> 1] = pack_bf16(p01.x, p01.y);
+            pk[(e >> 1) + 1] = pack_bf16(p23.x, p23.y);
           }
           tmem_st_32x32b_x16(tS + (c >> 1), pk);
         }
-        l += l0 + l1;
+        l += (la.x + la.y) + (lb.x + lb.y);
         tmem_wait_st();
         if (j > 0 && __any_sync(0xffffffffu, need)) {
           // Rescale the running O once the MMA that last accumulated into it is done.

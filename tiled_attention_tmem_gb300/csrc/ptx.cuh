@@ -74,6 +74,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Prefetches a 3-D tile into L2 (no shared-memory destination, no completion).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
 // Bulk (non-tensor) element-wise fp32 add of `bytes` from shared to global memory.
 __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, uint32_t bytes) {
   asm volatile(
@@ -202,14 +210,18 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
 //
 // K-major: tile rows are the M (or N) index, tile columns are K.  One MMA reads
 // 16 columns (32 bytes) inside one panel; rows advance by 1024 bytes per 8.
+//
+// Both views are built as the tile's base descriptor plus a byte offset added to
+// the start-address field, so unrolled K loops share one base computation.  The
+// field cannot overflow: shared-memory addresses stay below 256 KB.
 __device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, uint32_t panel_bytes, int k0) {
-  return make_sdesc(tile + (uint32_t)(k0 >> 6) * panel_bytes + (uint32_t)(k0 & 63) * 2u, 16u,
-                    1024u);
+  return make_sdesc(tile, 16u, 1024u) +
+         (uint64_t)(((uint32_t)(k0 >> 6) * panel_bytes + (uint32_t)(k0 & 63) * 2u) >> 4);
 }
 // MN-major: tile rows are K, tile columns are the M (or N) index.  One MMA reads
 // 16 rows (2048 bytes); the M/N extent advances one panel (panel_bytes) per 64.
 __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, uint32_t panel_bytes, int k0) {
-  return make_sdesc(tile + (uint32_t)k0 * 128u, panel_bytes, 1024u);
+  return make_sdesc(tile, panel_bytes, 1024u) + (uint64_t)(((uint32_t)k0 * 128u) >> 4);
 }
 
 __device__ __forceinline__ float ex2(float x) {
@@ -222,6 +234,17 @@ __device__ __forceinline__ float lg2(float x) {
   asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// Packed two-wide fp32 arithmetic (one instruction for two lanes of work).
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+
 // Two floats to packed bf16x2 (round to nearest even); `lo` lands in bits 0-15.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
