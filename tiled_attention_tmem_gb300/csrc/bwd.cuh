@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
     mbar_init(BAR(C::B_STGFREE), 1);
     mbar_init(BAR(C::B_STGFULL), 4);
     mbar_init(BAR(C::B_SCONS), 4);
-    mbar_init(BAR(C::B_DONE), 1);
+    mbar_init(BAR(C::B_DONE), C::EARLY ? 2 : 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -313,8 +313,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         for (int i = max(0, it - QS); i < it; ++i) wait_drain_bwd(BAR(C::B_QDFULL + i % QS), (i / QS) & 1);
       }
       __syncwarp();
-    } else if (warp == 1) {
+    } else if (warp == 1 || (C::EARLY && warp == 2)) {
       // ---------------------------------------------------------- MMA issue
+      // EARLY configurations use two issuing threads: warp 1 issues S^T / dP^T,
+      // warp 2 issues dV, dK and dQ.  The two streams touch disjoint TMEM columns
+      // and are ordered only through the compute warps' barriers, so a thread
+      // blocked on a commit or a wait no longer leaves the tensor pipe idle.
       if (lane == 0) {
         constexpr uint32_t idS = make_idesc(128, BM, false, false);
         constexpr uint32_t idAcc = make_idesc(128, DH, false, true);
@@ -360,28 +364,28 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           mma_commit(BAR(C::B_DQFULL));
         };
         bool ok = wait_one(BAR(C::B_KV), 0, ab, (kKBwdKV << 8) | 2);
-        if (ok && n > 0) {
+        if (ok && n > 0 && (!C::EARLY || warp == 1)) {
           ok = wait_one(BAR(C::B_QDFULL + 0), 0, ab, (kKBwdKV << 8) | 3);
           if (ok) {
             tc_fence_after();
             issue_sdp(0);
           }
         }
-        for (int i = 0; ok && i < n; ++i) {
-          const int s = i % QS;
-          if constexpr (C::EARLY) {
-            // S^T(i+1), dP^T(i+1) as soon as the compute warps hold S^T(i), dP^T(i) in registers.
-            if (i + 1 < n) {
-              const int s1 = (i + 1) % QS;
-              if (!wait_one(BAR(C::B_SCONS), i & 1, ab, (kKBwdKV << 8) | 14) ||
-                  !wait_one(BAR(C::B_QDFULL + s1), ((i + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              issue_sdp(s1);
+        if (C::EARLY && warp == 1) {
+          // S^T(i+1), dP^T(i+1) as soon as the compute warps hold S^T(i), dP^T(i) in registers.
+          for (int i = 0; ok && i + 1 < n; ++i) {
+            const int s1 = (i + 1) % QS;
+            if (!wait_one(BAR(C::B_SCONS), i & 1, ab, (kKBwdKV << 8) | 14) ||
+                !wait_one(BAR(C::B_QDFULL + s1), ((i + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
+              ok = false;
+              break;
             }
+            tc_fence_after();
+            issue_sdp(s1);
           }
+        }
+        for (int i = 0; ok && i < n && (!C::EARLY || warp == 2); ++i) {
+          const int s = i % QS;
           if (!wait_one(BAR(C::B_PDS), i & 1, ab, (kKBwdKV << 8) | 4)) {
             ok = false;
             break;
