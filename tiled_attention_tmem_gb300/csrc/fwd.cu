@@ -1,5 +1,7 @@
 // Forward launcher: tile configuration per head dimension and TMA descriptors.
 #include "fwd.cuh"
+#include <algorithm>
+
 #include "host.h"
 
 namespace fa {
@@ -37,9 +39,13 @@ fa_status run(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.causal = causal;
   const int n_qblk = (N + 128 * C::NQ - 1) / (128 * C::NQ);
   p.group = causal ? BH : head_group(n_qblk, BH);
-  const long long blocks = (long long)n_qblk * BH;
-  if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  return launch(FA_KERNEL_FWD, fwd_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  const long long items = (long long)n_qblk * BH;
+  if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  p.items = (int)items;
+  // Persistent grid: one CTA per SM (shared memory allows no more), each walking
+  // its share of the work items.
+  const long long grid = std::min<long long>(items, sm_count_cached());
+  return launch(FA_KERNEL_FWD, fwd_kernel<C>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, st, p);
 }
 
 }  // namespace

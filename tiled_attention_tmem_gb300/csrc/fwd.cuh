@@ -40,6 +40,7 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e)
   int causal;
   int group;  // heads per launch-order group
+  int items;  // work items (query blocks x heads); the grid is persistent over them
 };
 
 template <int D_, int NQ_, int BN_, int STAGES_>
@@ -58,7 +59,8 @@ struct FwdCfg {
   // barriers: q_full, kv_full[S], kv_empty[S], s_full[NQ], p_ready[NQ], o_ready[NQ], done
   static constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES,
                        B_SFULL = 1 + 2 * STAGES, B_PREADY = B_SFULL + NQ,
-                       B_OREADY = B_PREADY + NQ, B_DONE = B_OREADY + NQ, NBAR = B_DONE + 1;
+                       B_OREADY = B_PREADY + NQ, B_DONE = B_OREADY + NQ, B_QEMPTY = B_DONE + 1,
+                       NBAR = B_QEMPTY + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int TMEM_S = 0;         // S_t (and P_t aliased) at t*BN
@@ -114,6 +116,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
       mbar_init(bar0 + 8 * (C::B_OREADY + t), 1);
     }
     mbar_init(bar0 + 8 * C::B_DONE, 1);
+    mbar_init(bar0 + 8 * C::B_QEMPTY, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -126,20 +129,34 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
   const uint32_t tmem = *tmem_holder;
   const CtaAbort ab{abort_flag, p.err};
 
-  // Tile coordinates: causal launches walk query blocks from the last (the most
-  // key tiles) to the first so the longest CTAs of a head group start first.
+  // Persistent work loop.  Work item w is (query block, head) in launch order:
+  // heads grouped for L2 reuse, and under the causal mask the query blocks with
+  // the most key tiles first.  CTA c takes items in "snake" order over rounds
+  // (c, 2G-1-c, 2G+c, ...) so heavy and light items even out across CTAs.
+  // Barrier phases run on across items: every role counts the same iterations.
   const int n_qblk = (p.N + 128 * NQ - 1) / (128 * NQ);
-  int qb, bh;
-  grouped_order(blockIdx.x, n_qblk, p.BH, p.group, qb, bh);
-  if (p.causal) qb = n_qblk - 1 - qb;
-  const int q0 = qb * 128 * NQ;
-  int nkv[NQ];
-  int nmax = 0;
+  auto item_of = [&](int r) -> int {
+    const int G = gridDim.x, c = blockIdx.x;
+    return r * G + ((r & 1) ? (G - 1 - c) : c);
+  };
+  struct Item {
+    int q0, bh, nmax;
+    int nkv[NQ];
+  };
+  auto coords = [&](int w) {
+    Item it;
+    int qb;
+    grouped_order(w, n_qblk, p.BH, p.group, qb, it.bh);
+    if (p.causal) qb = n_qblk - 1 - qb;
+    it.q0 = qb * 128 * NQ;
+    it.nmax = 0;
 #pragma unroll
-  for (int t = 0; t < NQ; ++t) {
-    nkv[t] = fwd_kv_tiles(q0 + 128 * t, p.N, p.causal, BN);
-    nmax = max(nmax, nkv[t]);
-  }
+    for (int t = 0; t < NQ; ++t) {
+      it.nkv[t] = fwd_kv_tiles(it.q0 + 128 * t, p.N, p.causal, BN);
+      it.nmax = max(it.nmax, it.nkv[t]);
+    }
+    return it;
+  };
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
   // Two softmax warpgroups (384 threads, 168 registers each at launch): the
@@ -155,33 +172,42 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
         tma_prefetch_desc(&p.q_map);
         tma_prefetch_desc(&p.k_map);
         tma_prefetch_desc(&p.v_map);
-        mbar_expect_tx(BAR(C::B_QFULL), NQ * C::Q_TILE);
-        for (int t = 0; t < NQ; ++t)
-          for (int pn = 0; pn < C::PANELS; ++pn)
-            tma_load_3d(sbase + C::OFF_Q + t * C::Q_TILE + pn * C::Q_PANEL, &p.q_map,
-                        BAR(C::B_QFULL), 64 * pn, q0 + 128 * t, bh);
-        int it = 0;
+        int it = 0, nitems = 0;
         bool ok = true;
-        for (int j = 0; j < nmax && ok; ++j) {
-          for (int w = 0; w < 2; ++w) {
-            const int s = it % S;
-            if (!wait_one(BAR(C::B_KVEMPTY + s), ((it / S) & 1) ^ 1, ab, (kKFwd << 8) | 1)) {
-              ok = false;
-              break;
-            }
-            mbar_expect_tx(BAR(C::B_KVFULL + s), C::KV_TILE);
-            const CUtensorMap* m = w ? &p.v_map : &p.k_map;
+        for (int r = 0; ok; ++r) {
+          const int w = item_of(r);
+          if (w >= p.items) break;
+          const Item I = coords(w);
+          // The previous item's S MMAs must be done reading Q.
+          if (!wait_one(BAR(C::B_QEMPTY), (nitems & 1) ^ 1, ab, (kKFwd << 8) | 10)) break;
+          mbar_expect_tx(BAR(C::B_QFULL), NQ * C::Q_TILE);
+          for (int t = 0; t < NQ; ++t)
             for (int pn = 0; pn < C::PANELS; ++pn)
-              tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m,
-                          BAR(C::B_KVFULL + s), 64 * pn, j * BN, bh);
-            // Pull K/V tiles a few steps beyond the ring into L2.
-            if (j + C::PREFETCH < nmax)
-              for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(m, 64 * pn, (j + C::PREFETCH) * BN, bh);
-            ++it;
+              tma_load_3d(sbase + C::OFF_Q + t * C::Q_TILE + pn * C::Q_PANEL, &p.q_map, BAR(C::B_QFULL), 64 * pn,
+                          I.q0 + 128 * t, I.bh);
+          ++nitems;
+          for (int j = 0; j < I.nmax && ok; ++j) {
+            for (int wkv = 0; wkv < 2; ++wkv) {
+              const int s = it % S;
+              if (!wait_one(BAR(C::B_KVEMPTY + s), ((it / S) & 1) ^ 1, ab, (kKFwd << 8) | 1)) {
+                ok = false;
+                break;
+              }
+              mbar_expect_tx(BAR(C::B_KVFULL + s), C::KV_TILE);
+              const CUtensorMap* m = wkv ? &p.v_map : &p.k_map;
+              for (int pn = 0; pn < C::PANELS; ++pn)
+                tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m, BAR(C::B_KVFULL + s),
+                            64 * pn, j * BN, I.bh);
+              // Pull K/V tiles a few steps beyond the ring into L2.
+              if (j + C::PREFETCH < I.nmax)
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                  tma_prefetch_l2_3d(m, 64 * pn, (j + C::PREFETCH) * BN, I.bh);
+              ++it;
+            }
           }
         }
         // Let every copy this thread started land before the CTA can exit.
-        wait_drain(BAR(C::B_QFULL), 0);
+        if (nitems > 0) wait_drain(BAR(C::B_QFULL), (nitems - 1) & 1);
         for (int i = max(0, it - S); i < it; ++i) wait_drain(BAR(C::B_KVFULL + i % S), (i / S) & 1);
       }
       __syncwarp();
@@ -199,59 +225,74 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
                    desc_kmajor(kb, C::KV_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
           mma_commit(BAR(C::B_SFULL + t));
         };
-        bool ok = wait_one(BAR(C::B_QFULL), 0, ab, (kKFwd << 8) | 2);
-        int it = 0;
-        if (ok && nmax > 0) {
-          const int s = it % S;
-          ok = wait_one(BAR(C::B_KVFULL + s), (it / S) & 1, ab, (kKFwd << 8) | 3);
-          if (ok) {
+        int it = 0, nitems = 0;
+        int g[NQ];
+#pragma unroll
+        for (int t = 0; t < NQ; ++t) g[t] = 0;
+        bool ok = true;
+        for (int r = 0; ok; ++r) {
+          const int w = item_of(r);
+          if (w >= p.items) break;
+          const Item I = coords(w);
+          ok = wait_one(BAR(C::B_QFULL), nitems & 1, ab, (kKFwd << 8) | 2);
+          ++nitems;
+          if (!ok) break;
+          {
+            const int s = it % S;
+            ok = wait_one(BAR(C::B_KVFULL + s), (it / S) & 1, ab, (kKFwd << 8) | 3);
+            if (!ok) break;
             tc_fence_after();
             for (int t = 0; t < NQ; ++t)
-              if (nkv[t] > 0) issue_s(t, s);
+              if (I.nkv[t] > 0) issue_s(t, s);
             mma_commit(BAR(C::B_KVEMPTY + s));
+            if (I.nmax == 1) mma_commit(BAR(C::B_QEMPTY));
             ++it;
           }
-        }
-        for (int j = 0; ok && j < nmax; ++j) {
-          const int sv = it % S;
-          ok = wait_one(BAR(C::B_KVFULL + sv), (it / S) & 1, ab, (kKFwd << 8) | 4);
-          ++it;
-          if (!ok) break;
-          tc_fence_after();
-          const int sk = it % S;
-          bool k_ready = false;
-          const uint32_t vb = sbase + C::OFF_KV + sv * C::KV_TILE;
-          for (int t = 0; t < NQ && ok; ++t) {
-            if (j < nkv[t]) {
-              if (!wait_one(BAR(C::B_PREADY + t), j & 1, ab, (kKFwd << 8) | 5)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-#pragma unroll
-              for (int k = 0; k < BN / 16; ++k)
-                mma_ts(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * BN + 8 * k,
-                       desc_mnmajor(vb, C::KV_PANEL, 16 * k), idO, (j > 0 || k > 0) ? 1u : 0u);
-              mma_commit(BAR(C::B_OREADY + t));
-            }
-            if (j + 1 < nkv[t]) {
-              if (!k_ready) {
-                if (!wait_one(BAR(C::B_KVFULL + sk), (it / S) & 1, ab, (kKFwd << 8) | 6)) {
+          for (int j = 0; ok && j < I.nmax; ++j) {
+            const int sv = it % S;
+            ok = wait_one(BAR(C::B_KVFULL + sv), (it / S) & 1, ab, (kKFwd << 8) | 4);
+            ++it;
+            if (!ok) break;
+            tc_fence_after();
+            const int sk = it % S;
+            bool k_ready = false;
+            const uint32_t vb = sbase + C::OFF_KV + sv * C::KV_TILE;
+            for (int t = 0; t < NQ && ok; ++t) {
+              if (j < I.nkv[t]) {
+                if (!wait_one(BAR(C::B_PREADY + t), (g[t] + j) & 1, ab, (kKFwd << 8) | 5)) {
                   ok = false;
                   break;
                 }
                 tc_fence_after();
-                k_ready = true;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k)
+                  mma_ts(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * BN + 8 * k,
+                         desc_mnmajor(vb, C::KV_PANEL, 16 * k), idO, (j > 0 || k > 0) ? 1u : 0u);
+                mma_commit(BAR(C::B_OREADY + t));
               }
-              issue_s(t, sk);
+              if (j + 1 < I.nkv[t]) {
+                if (!k_ready) {
+                  if (!wait_one(BAR(C::B_KVFULL + sk), (it / S) & 1, ab, (kKFwd << 8) | 6)) {
+                    ok = false;
+                    break;
+                  }
+                  tc_fence_after();
+                  k_ready = true;
+                }
+                issue_s(t, sk);
+              }
             }
+            if (!ok) break;
+            mma_commit(BAR(C::B_KVEMPTY + sv));
+            if (k_ready) {
+              mma_commit(BAR(C::B_KVEMPTY + sk));
+              ++it;
+            }
+            // The item's last S MMAs have been issued: Q may be reloaded once they finish.
+            if (j + 2 == I.nmax) mma_commit(BAR(C::B_QEMPTY));
           }
-          if (!ok) break;
-          mma_commit(BAR(C::B_KVEMPTY + sv));
-          if (k_ready) {
-            mma_commit(BAR(C::B_KVEMPTY + sk));
-            ++it;
-          }
+#pragma unroll
+          for (int t = 0; t < NQ; ++t) g[t] += I.nkv[t];
         }
         // Every MMA issued above must finish before TMEM is released.
         mma_commit(BAR(C::B_DONE));
@@ -265,98 +306,108 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
       const int t = (warp - 4) >> 2;
       const int quad = warp & 3;
       const int r = quad * 32 + lane;
-      const int qi = q0 + 128 * t + r;
-      const int n = nkv[t];
-      const int limit = p.causal ? min(qi, p.N - 1) : p.N - 1;
       const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
       const uint32_t tS = trow + C::TMEM_S + t * BN;
       const uint32_t tO = trow + C::TMEM_O + t * D;
       const float cs = p.scale_log2;
-      float m_used = -INFINITY;
-      float l = 0.f;
+      int g = 0;  // iterations of this query tile in earlier items
       bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        if (!wait_warp(BAR(C::B_SFULL + t), j & 1, ab, (kKFwd << 8) | 7)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        uint32_t sr[BN];
-#pragma unroll
-        for (int c = 0; c < BN; c += 32) tmem_ld_32x32b_x32(tS + c, sr + c);
-        tmem_wait_ld();
-        reg_fence<BN>(sr);
-        const int kbase = j * BN;
-        if (kbase + BN - 1 > limit) {
-#pragma unroll
-          for (int c = 0; c < BN; ++c)
-            if (kbase + c > limit) sr[c] = __float_as_uint(-INFINITY);
-        }
-        // Row maximum: four independent chains of three-input max.
-        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < BN; c += 8) {
-          mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-          mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-          mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-          mx3 = max3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
-        }
-        const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs;
-        const bool need = m_cand > m_used + 8.0f;
-        float alpha = 1.f;
-        if (need) {
-          alpha = ex2(m_used - m_cand);
-          m_used = m_cand;
-          l *= alpha;
-        }
-        const float msub = (m_used == -INFINITY) ? 0.f : m_used;
-        // p = exp2(s * c - m), two columns per packed FMA / add.
-        const float2 c2 = make_float2(cs, cs), nm2 = make_float2(-msub, -msub);
-        float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int c = 0; c < BN; c += 32) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float2 x01 = ffma2(make_float2(__uint_as_float(sr[c + e]), __uint_as_float(sr[c + e + 1])), c2, nm2);
-            const float2 x23 =
-                ffma2(make_float2(__uint_as_float(sr[c + e + 2]), __uint_as_float(sr[c + e + 3])), c2, nm2);
-            const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
-            const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
-            la = fadd2(la, p01);
-            lb = fadd2(lb, p23);
-            pk[e >> 1] = pack_bf16(p01.x, p01.y);
-            pk[(e >> 1) + 1] = pack_bf16(p23.x, p23.y);
-          }
-          tmem_st_32x32b_x16(tS + (c >> 1), pk);
-        }
-        l += (la.x + la.y) + (lb.x + lb.y);
-        tmem_wait_st();
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-          // Rescale the running O once the MMA that last accumulated into it is done.
-          if (!wait_warp(BAR(C::B_OREADY + t), (j - 1) & 1, ab, (kKFwd << 8) | 8)) {
+      for (int rr = 0; ok; ++rr) {
+        const int w = item_of(rr);
+        if (w >= p.items) break;
+        const Item I = coords(w);
+        const int qi = I.q0 + 128 * t + r;
+        const int n = I.nkv[t];
+        const int bh = I.bh;
+        const int limit = p.causal ? min(qi, p.N - 1) : p.N - 1;
+        float m_used = -INFINITY;
+        float l = 0.f;
+        for (int j = 0; j < n; ++j) {
+          if (!wait_warp(BAR(C::B_SFULL + t), (g + j) & 1, ab, (kKFwd << 8) | 7)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          uint32_t sr[BN];
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t orr[32];
-            tmem_ld_32x32b_x32(tO + c0, orr);
-            tmem_wait_ld();
-            reg_fence<32>(orr);
+          for (int c = 0; c < BN; c += 32) tmem_ld_32x32b_x32(tS + c, sr + c);
+          tmem_wait_ld();
+          reg_fence<BN>(sr);
+          const int kbase = j * BN;
+          if (kbase + BN - 1 > limit) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
-            tmem_st_32x32b_x32(tO + c0, orr);
+            for (int c = 0; c < BN; ++c)
+              if (kbase + c > limit) sr[c] = __float_as_uint(-INFINITY);
           }
+          // Row maximum: four independent chains of three-input max.
+          float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < BN; c += 8) {
+            mx0 = max3(mx0, __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+            mx1 = max3(mx1, __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+            mx2 = max3(mx2, __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+            mx3 = max3(mx3, __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+          }
+          const float m_cand = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * cs;
+          const bool need = m_cand > m_used + 8.0f;
+          float alpha = 1.f;
+          if (need) {
+            alpha = ex2(m_used - m_cand);
+            m_used = m_cand;
+            l *= alpha;
+          }
+          const float msub = (m_used == -INFINITY) ? 0.f : m_used;
+          // p = exp2(s * c - m), two columns per packed FMA / add.
+          const float2 c2 = make_float2(cs, cs), nm2 = make_float2(-msub, -msub);
+          float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int c = 0; c < BN; c += 32) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float2 x01 =
+                  ffma2(make_float2(__uint_as_float(sr[c + e]), __uint_as_float(sr[c + e + 1])), c2, nm2);
+              const float2 x23 =
+                  ffma2(make_float2(__uint_as_float(sr[c + e + 2]), __uint_as_float(sr[c + e + 3])), c2, nm2);
+              const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+              const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+              la = fadd2(la, p01);
+              lb = fadd2(lb, p23);
+              pk[e >> 1] = pack_bf16(p01.x, p01.y);
+              pk[(e >> 1) + 1] = pack_bf16(p23.x, p23.y);
+            }
+            tmem_st_32x32b_x16(tS + (c >> 1), pk);
+          }
+          l += (la.x + la.y) + (lb.x + lb.y);
           tmem_wait_st();
+          if (j > 0 && __any_sync(0xffffffffu, need)) {
+            // Rescale the running O once the MMA that last accumulated into it is done.
+            if (!wait_warp(BAR(C::B_OREADY + t), (g + j - 1) & 1, ab, (kKFwd << 8) | 8)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t orr[32];
+              tmem_ld_32x32b_x32(tO + c0, orr);
+              tmem_wait_ld();
+              reg_fence<32>(orr);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) orr[e] = __float_as_uint(__uint_as_float(orr[e]) * alpha);
+              tmem_st_32x32b_x32(tO + c0, orr);
+            }
+            tmem_wait_st();
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(C::B_PREADY + t));
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(C::B_PREADY + t));
-      }
-      if (ok && n > 0) {
-        if (wait_warp(BAR(C::B_OREADY + t), (n - 1) & 1, ab, (kKFwd << 8) | 9)) {
+        if (ok && n > 0) {
+          if (!wait_warp(BAR(C::B_OREADY + t), (g + n - 1) & 1, ab, (kKFwd << 8) | 9)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
           const float inv = 1.f / l;
           const bool store = qi < p.N;
@@ -380,6 +431,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           }
           if (store) p.lse[(size_t)bh * p.N + qi] = (m_used + log2f(l)) * kLn2;
         }
+        g += n;
       }
     }
   }

@@ -67,7 +67,7 @@ int* device_error_word() {
   return g_err_word[dev];
 }
 
-int head_group(int tiles_per_head, int BH) {
+int sm_count_cached() {
   static int sms[kMaxDevices] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
@@ -76,8 +76,12 @@ int head_group(int tiles_per_head, int BH) {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
     sms[dev] = n;
   }
+  return sms[dev];
+}
+
+int head_group(int tiles_per_head, int BH) {
   const int t = tiles_per_head > 0 ? tiles_per_head : 1;
-  const int g = (2 * sms[dev] + t - 1) / t;
+  const int g = (2 * sm_count_cached() + t - 1) / t;
   return g < 1 ? 1 : (g > BH ? BH : g);
 }
 

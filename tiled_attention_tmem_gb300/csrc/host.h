@@ -26,6 +26,9 @@ fa_status make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType 
 // better than locality helps.
 int head_group(int tiles_per_head, int BH);
 
+// Multiprocessor count of the current device (cached per device).
+int sm_count_cached();
+
 // Profiling markers (no-ops unless fa_profile_start is active).
 void prof_before(int kind, cudaStream_t st);
 void prof_after(int kind, cudaStream_t st);
