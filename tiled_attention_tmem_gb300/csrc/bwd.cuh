@@ -161,6 +161,12 @@ struct BwdKVCfg {
   // EARLY: the compute warps load all of S^T / dP^T into registers and release
   // those TMEM columns at once, so S^T(i+1), dP^T(i+1) run during the softmax of i.
   static constexpr bool EARLY = SEP && BM == 64;
+  // Compute warpgroups: the 5-GEMM EARLY kernel splits the BM query columns
+  // (and the dV / dK epilogue) over two warpgroups to halve the per-tile
+  // critical path; the 7-GEMM kernel measured faster with one.
+  static constexpr int NCW = (EARLY && DQ) ? 2 : 1;
+  static constexpr int CW = BM / NCW;
+  static constexpr int DRAIN_W0 = 4 + 4 * NCW;  // first dQ drain warp (5-GEMM)
   static constexpr bool DQ_T = DQ && D == 128;  // dQ^T (lanes = d) vs dQ (lanes = query)
   static constexpr int BN = 128;
   static constexpr int DH = D / DSPLIT;
@@ -198,7 +204,11 @@ struct BwdKVCfg {
   static constexpr int DQ_COLS = DQ ? (DQ_T ? BM : D) : 0;
   static constexpr int TMEM_USED = T_DQ + DQ_COLS;
   static constexpr uint32_t TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
-  static constexpr int THREADS = DQ ? 384 : 256;
+  static constexpr int THREADS = 128 * (1 + NCW + (DQ ? 1 : 0));
+  // setmaxnreg budgets per warpgroup (producer/MMA, compute; the drain keeps the
+  // launch budget): the sum over warpgroups stays within THREADS * (65536 / THREADS).
+  static constexpr int REG_LOW = THREADS == 512 ? 64 : 80;
+  static constexpr int REG_COMPUTE = THREADS == 512 ? 160 : (NCW == 2 ? 208 : 224);
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(!SEP || QS >= 2, "overlapped order needs two query stages");
@@ -229,13 +239,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
       mbar_init(BAR(C::B_QDEMPTY + s), 1);
     }
     mbar_init(BAR(C::B_SDP), 1);
-    mbar_init(BAR(C::B_PDS), 4);
+    mbar_init(BAR(C::B_PDS), 4 * C::NCW);
     mbar_init(BAR(C::B_MMA), 1);
     mbar_init(BAR(C::B_DQFULL), 1);
     mbar_init(BAR(C::B_DQFREE), 4);
     mbar_init(BAR(C::B_STGFREE), 1);
     mbar_init(BAR(C::B_STGFULL), 4);
-    mbar_init(BAR(C::B_SCONS), 4);
+    mbar_init(BAR(C::B_SCONS), 4 * C::NCW);
     mbar_init(BAR(C::B_DONE), C::EARLY ? 2 : 1);
     fence_mbar_init();
   }
@@ -271,10 +281,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
   // starts with its warpgroup's register budget.  The producer/MMA warpgroup
   // gives registers to the compute warpgroup; 128 * (80 + 224 + 168) stays
   // within the 384 * 168 the block was launched with.
-  constexpr bool kSplitRegs = C::THREADS == 384;
+  constexpr bool kSplitRegs = C::THREADS >= 384;
   if (!*abort_flag) {
     if (warp < 4) {
-    if constexpr (kSplitRegs) regs_shrink<80>();
+    if constexpr (kSplitRegs) regs_shrink<C::REG_LOW>();
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
@@ -430,9 +440,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
       }
       __syncwarp();
     }
-    } else if (warp < 8) {
+    } else if (warp < C::DRAIN_W0) {
       // ---------------------------------------------- P^T / dS^T (thread = key row)
-      if constexpr (kSplitRegs) regs_grow<224>();
+      if constexpr (kSplitRegs) regs_grow<C::REG_COMPUTE>();
+      const int cw = (warp - 4) >> 2;      // compute warpgroup: query columns [c_lo, c_lo + CW)
+      const int c_lo = cw * C::CW;
       const int quad = warp & 3;
       const int r = quad * 32 + lane;
       const int kj = k0 + r;
@@ -469,7 +481,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
             }
           }
         };
-        constexpr int HOLD = C::SEP ? BM / 2 : 16;
+        constexpr int HOLD = C::SEP ? C::CW / 2 : 16;
         uint32_t pk_p[HOLD], pk_ds[HOLD];
         // P^T = exp2(S^T c - lse2), dS^T = P^T (dP^T - D) for columns [c0, c0 + 32).
         const float2 c2 = make_float2(cs, cs);
@@ -504,20 +516,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           }
         };
         if constexpr (C::EARLY) {
-          uint32_t sr[BM], dr[BM];
+          uint32_t sr[C::CW], dr[C::CW];
 #pragma unroll
-          for (int c0 = 0; c0 < BM; c0 += 32) {
-            tmem_ld_32x32b_x32(trow + C::T_ST + c0, sr + c0);
-            tmem_ld_32x32b_x32(trow + C::T_DPT + c0, dr + c0);
+          for (int c0 = 0; c0 < C::CW; c0 += 32) {
+            tmem_ld_32x32b_x32(trow + C::T_ST + c_lo + c0, sr + c0);
+            tmem_ld_32x32b_x32(trow + C::T_DPT + c_lo + c0, dr + c0);
           }
           tmem_wait_ld();
-          reg_fence<BM>(sr);
-          reg_fence<BM>(dr);
+          reg_fence<C::CW>(sr);
+          reg_fence<C::CW>(dr);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(C::B_SCONS));
 #pragma unroll
-          for (int c0 = 0; c0 < BM; c0 += 32) compute_chunk(c0, sr + c0, dr + c0, c0 >> 1);
+          for (int c0 = 0; c0 < C::CW; c0 += 32) compute_chunk(c_lo + c0, sr + c0, dr + c0, c0 >> 1);
         } else {
 #pragma unroll
           for (int c0 = 0; c0 < BM; c0 += 32) {
@@ -539,7 +551,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           }
           tc_fence_after();
 #pragma unroll
-          for (int c0 = 0; c0 < BM; c0 += 32) store_chunk(c0, pk_p + (c0 >> 1), pk_ds + (c0 >> 1));
+          for (int c0 = 0; c0 < C::CW; c0 += 32) store_chunk(c_lo + c0, pk_p + (c0 >> 1), pk_ds + (c0 >> 1));
         }
         if constexpr (C::DQ) fence_proxy_async_smem();
         tmem_wait_st();
@@ -554,6 +566,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         const size_t rowoff = ((size_t)bh * p.N + (size_t)(store ? kj : 0)) * D + h * DH;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
+          if (C::NCW == 2 && which != cw) continue;  // two warpgroups: one stores dV, the other dK
           uint16_t* dst = (which == 0 ? p.dv : p.dk) + rowoff;
           const float mul = which == 0 ? 1.f : p.scale;
           const uint32_t tacc = trow + (which == 0 ? C::T_DV : C::T_DK);
@@ -574,21 +587,21 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
             }
           }
         }
-      } else if (n == 0 && key_ok) {
+      } else if (n == 0 && key_ok && cw == 0) {
         // No query can see this key (possible only with ragged tails): zero gradients.
         for (int c = 0; c < DH; c += 8) {
           *reinterpret_cast<uint4*>(p.dv + ((size_t)bh * p.N + kj) * D + h * DH + c) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(p.dk + ((size_t)bh * p.N + kj) * D + h * DH + c) = make_uint4(0, 0, 0, 0);
         }
       }
-    } else if (warp >= 8) {
+    } else {
       if constexpr (C::DQ) {
       // ------------------------------------------------------ dQ drain (5-GEMM)
       const int quad = warp & 3;
       const int lr = quad * 32 + lane;  // TMEM lane: d index (dQ^T) or query row (dQ)
       const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16) + C::T_DQ;
       float* stg = reinterpret_cast<float*>(gbase + C::OFF_STG);
-      const bool leader = (warp == 8 && lane == 0);
+      const bool leader = (warp == C::DRAIN_W0 && lane == 0);
       for (int i = 0; i < n; ++i) {
         if (!wait_warp(BAR(C::B_DQFULL), i & 1, ab, (kKBwdKV << 8) | 11)) break;
         tc_fence_after();
