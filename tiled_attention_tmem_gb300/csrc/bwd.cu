@@ -95,9 +95,13 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
   p.scale = scale;
   p.causal = causal;
   p.group = causal ? BH : head_group(((N + C::BN - 1) / C::BN) * C::DSPLIT, BH);
-  const long long blocks = (long long)((N + C::BN - 1) / C::BN) * BH * C::DSPLIT;
-  if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  return launch(C::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  const long long items = (long long)((N + C::BN - 1) / C::BN) * BH * C::DSPLIT;
+  if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  p.items = (int)items;
+  // Persistent grid: one CTA per SM (one fits per SM), each walking its items.
+  const long long grid = std::min<long long>(items, sm_count_cached());
+  return launch(C::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<C>, dim3((unsigned)grid),
+                dim3(C::THREADS), C::SMEM_BYTES, st, p);
 }
 
 template <class C>

@@ -119,9 +119,10 @@ __global__ void __launch_bounds__(256) bwd_conv_kernel(const ConvParams p) {
 }
 
 // ------------------------------------------------------------ dK/dV kernel
-// CTA = one tile of 128 keys (the MMA M dimension for S^T, dP^T, dV, dK) of one
-// head, walking the query tiles of BM rows that can see it.  With DSPLIT = 2
-// each of two CTAs keeps half of the d columns of dV and dK (head dim 256).
+// Work item = one tile of 128 keys (the MMA M dimension for S^T, dP^T, dV, dK)
+// of one head, walking the query tiles of BM rows that can see it; one
+// persistent CTA per SM runs items back to back.  With DSPLIT = 2 each of two
+// items keeps half of the d columns of dV and dK (head dim 256).
 //
 //   S^T  = K Q^T     (A = K K-major, B = Q K-major)          -> TMEM fp32
 //   dP^T = V dO^T    (A = V K-major, B = dO K-major)          -> TMEM fp32
@@ -152,6 +153,7 @@ struct BwdKVParams {
   float scale;
   int causal;
   int group;  // heads per launch-order group
+  int items;  // work items (key tiles x d parts x heads); the grid is persistent over them
 };
 
 template <int D_, int BM_, bool DQ_, int DSPLIT_, int QS_, bool SEP_>
@@ -192,7 +194,8 @@ struct BwdKVCfg {
   static constexpr int B_KV = 0, B_QDFULL = 1, B_QDEMPTY = 1 + QS, B_SDP = 1 + 2 * QS,
                        B_PDS = B_SDP + 1, B_MMA = B_PDS + 1, B_DQFULL = B_MMA + 1,
                        B_DQFREE = B_DQFULL + 1, B_STGFREE = B_DQFREE + 1, B_STGFULL = B_STGFREE + 1,
-                       B_SCONS = B_STGFULL + 1, B_DONE = B_SCONS + 1, NBAR = B_DONE + 1;
+                       B_SCONS = B_STGFULL + 1, B_DONE = B_SCONS + 1, B_KVEMPTY = B_DONE + 1,
+                       NBAR = B_KVEMPTY + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
   // TMEM columns
@@ -205,10 +208,15 @@ struct BwdKVCfg {
   static constexpr int TMEM_USED = T_DQ + DQ_COLS;
   static constexpr uint32_t TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
   static constexpr int THREADS = 128 * (1 + NCW + (DQ ? 1 : 0));
-  // setmaxnreg budgets per warpgroup (producer/MMA, compute; the drain keeps the
-  // launch budget): the sum over warpgroups stays within THREADS * (65536 / THREADS).
-  static constexpr int REG_LOW = THREADS == 512 ? 64 : 80;
+  // setmaxnreg budgets per warpgroup (producer/MMA, compute, dQ drain): the sum
+  // over warpgroups stays within the launch's THREADS * (65536 / THREADS),
+  // i.e. 72 + 2 * 160 + 120 = 512 at 512 threads and 96 + 224 + 168 <= 3 * 168.
+  static constexpr int REG_LAUNCH = 65536 / THREADS >= 256 ? 255 : (65536 / THREADS) / 8 * 8;
+  static constexpr int REG_LOW = THREADS == 512 ? 72 : 96;
   static constexpr int REG_COMPUTE = THREADS == 512 ? 160 : (NCW == 2 ? 208 : 224);
+  static constexpr int REG_DRAIN = THREADS == 512 ? 120 : REG_LAUNCH;
+  static_assert(THREADS < 384 || REG_LOW + NCW * REG_COMPUTE + (DQ ? REG_DRAIN : 0) <= THREADS / 128 * REG_LAUNCH,
+                "register split exceeds the launch budget");
   static_assert(TMEM_USED <= 512, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(!SEP || QS >= 2, "overlapped order needs two query stages");
@@ -234,6 +242,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
   if (threadIdx.x == 0) {
     *abort_flag = (*reinterpret_cast<volatile int*>(p.err) != 0) ? 1 : 0;
     mbar_init(BAR(C::B_KV), 1);
+    mbar_init(BAR(C::B_KVEMPTY), C::EARLY ? 2 : 1);
     for (int s = 0; s < QS; ++s) {
       mbar_init(BAR(C::B_QDFULL + s), 1);
       mbar_init(BAR(C::B_QDEMPTY + s), 1);
@@ -259,18 +268,31 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
   const uint32_t tmem = *tmem_holder;
   const CtaAbort ab{abort_flag, p.err};
 
-  // Tile coordinates: key tile kb (natural order: under the causal mask the
-  // first key tiles see the most query tiles and start first), head bh, d part h.
-  int tile, bh;
-  grouped_order(blockIdx.x, ((p.N + C::BN - 1) / C::BN) * C::DSPLIT, p.BH, p.group, tile, bh);
-  const int kb = tile / C::DSPLIT;
-  const int h = tile % C::DSPLIT;
-  const int k0 = kb * C::BN;
+  // Persistent work loop.  Work item w = (key tile, d part, head) in launch
+  // order: under the causal mask the key tiles that the most query tiles see
+  // come first, heads varying fastest; without it heads are grouped for L2
+  // reuse.  CTA c takes items in snake order over rounds (c, 2G-1-c, 2G+c, ...)
+  // so heavy and light items even out.  Every role walks the same items and
+  // counts the same query tiles, so barrier phases run on across items.
+  const int n_kt = (p.N + C::BN - 1) / C::BN;
   const int n_qt = (p.N + BM - 1) / BM;
-  const int qt0 = p.causal ? k0 / BM : 0;
-  const int n = n_qt - qt0;
-  const float* lse2_g = p.lse2 + (size_t)bh * p.Npad;
-  const float* dd_g = p.dd + (size_t)bh * p.Npad;
+  auto item_of = [&](int r) -> int {
+    const int G = gridDim.x, c = blockIdx.x;
+    return r * G + ((r & 1) ? (G - 1 - c) : c);
+  };
+  struct Item {
+    int bh, h, k0, qt0, n;  // head, d part, first key, first query tile, query tiles
+  };
+  auto coords = [&](int w) {
+    Item I;
+    int tile;
+    grouped_order(w, n_kt * C::DSPLIT, p.BH, p.group, tile, I.bh);
+    I.h = tile % C::DSPLIT;
+    I.k0 = (tile / C::DSPLIT) * C::BN;
+    I.qt0 = p.causal ? I.k0 / BM : 0;
+    I.n = n_qt - I.qt0;
+    return I;
+  };
 
   auto stage_q = [&](int s) { return sbase + C::OFF_STAGE + s * C::STAGE_BYTES; };
   auto stage_do = [&](int s) { return stage_q(s) + C::QD_TILE; };
@@ -287,40 +309,70 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
     if constexpr (kSplitRegs) regs_shrink<C::REG_LOW>();
     if (warp == 0) {
       // ------------------------------------------------------------ producer
+      // Query-tile stages run on across items.  An item's first stages are
+      // issued before its K/V tile, which has to wait until the previous
+      // item's last MMAs have read K and V.
       if (lane == 0) {
         tma_prefetch_desc(&p.q_map);
         tma_prefetch_desc(&p.k_map);
         tma_prefetch_desc(&p.v_map);
         tma_prefetch_desc(&p.do_map);
-        mbar_expect_tx(BAR(C::B_KV), 2 * C::KV_TILE);
-        for (int pn = 0; pn < C::PANELS; ++pn) {
-          tma_load_3d(sbase + C::OFF_K + pn * C::KV_PANEL, &p.k_map, BAR(C::B_KV), 64 * pn, k0, bh);
-          tma_load_3d(sbase + C::OFF_V + pn * C::KV_PANEL, &p.v_map, BAR(C::B_KV), 64 * pn, k0, bh);
-        }
-        int it = 0;
-        for (; it < n; ++it) {
-          const int s = it % QS;
-          if (!wait_one(BAR(C::B_QDEMPTY + s), ((it / QS) & 1) ^ 1, ab, (kKBwdKV << 8) | 1)) break;
-          const int qrow = (qt0 + it) * BM;
-          mbar_expect_tx(BAR(C::B_QDFULL + s), C::STAGE_TX);
+        int it = 0, nkv = 0;
+        bool ok = true;
+        auto prefetch_qd = [&](const Item& I, int i) {
+          const int prow = (I.qt0 + i) * BM;
           for (int pn = 0; pn < C::PANELS; ++pn) {
-            tma_load_3d(stage_q(s) + pn * C::QD_PANEL, &p.q_map, BAR(C::B_QDFULL + s), 64 * pn, qrow, bh);
-            tma_load_3d(stage_do(s) + pn * C::QD_PANEL, &p.do_map, BAR(C::B_QDFULL + s), 64 * pn, qrow, bh);
+            tma_prefetch_l2_3d(&p.q_map, 64 * pn, prow, I.bh);
+            tma_prefetch_l2_3d(&p.do_map, 64 * pn, prow, I.bh);
           }
-          bulk_load(stage_lse(s), lse2_g + qrow, BM * 4, BAR(C::B_QDFULL + s));
-          bulk_load(stage_dd(s), dd_g + qrow, BM * 4, BAR(C::B_QDFULL + s));
-          // Stage loads can only start once a slot frees up (about two tiles ahead of
-          // use); pull the tiles further ahead into L2 so those loads hit L2.
-          if (it + C::PREFETCH < n) {
-            const int prow = (qt0 + it + C::PREFETCH) * BM;
+        };
+        for (int r = 0; ok; ++r) {
+          const int w = item_of(r);
+          if (w >= p.items) break;
+          const Item I = coords(w);
+          if (I.n <= 0) continue;
+          const int wn = item_of(r + 1);
+          const bool has_next = wn < p.items;
+          const Item J = has_next ? coords(wn) : I;
+          auto issue_stage = [&](int i) -> bool {
+            const int s = it % QS;
+            if (!wait_one(BAR(C::B_QDEMPTY + s), ((it / QS) & 1) ^ 1, ab, (kKBwdKV << 8) | 1)) return false;
+            const int qrow = (I.qt0 + i) * BM;
+            mbar_expect_tx(BAR(C::B_QDFULL + s), C::STAGE_TX);
             for (int pn = 0; pn < C::PANELS; ++pn) {
-              tma_prefetch_l2_3d(&p.q_map, 64 * pn, prow, bh);
-              tma_prefetch_l2_3d(&p.do_map, 64 * pn, prow, bh);
+              tma_load_3d(stage_q(s) + pn * C::QD_PANEL, &p.q_map, BAR(C::B_QDFULL + s), 64 * pn, qrow, I.bh);
+              tma_load_3d(stage_do(s) + pn * C::QD_PANEL, &p.do_map, BAR(C::B_QDFULL + s), 64 * pn, qrow, I.bh);
             }
+            bulk_load(stage_lse(s), p.lse2 + (size_t)I.bh * p.Npad + qrow, BM * 4, BAR(C::B_QDFULL + s));
+            bulk_load(stage_dd(s), p.dd + (size_t)I.bh * p.Npad + qrow, BM * 4, BAR(C::B_QDFULL + s));
+            ++it;
+            // Stage loads can only start once a slot frees up (a few tiles ahead of
+            // use); pull the tiles further ahead, into the next item, into L2.
+            const int ahead = i + C::PREFETCH;
+            if (ahead < I.n) prefetch_qd(I, ahead);
+            else if (has_next && ahead - I.n < J.n) prefetch_qd(J, ahead - I.n);
+            return true;
+          };
+          const int pre = min(QS - 1, I.n);
+          int i = 0;
+          for (; ok && i < pre; ++i) ok = issue_stage(i);
+          if (!ok) break;
+          if (nkv > 0 && !wait_one(BAR(C::B_KVEMPTY), (nkv - 1) & 1, ab, (kKBwdKV << 8) | 15)) break;
+          mbar_expect_tx(BAR(C::B_KV), 2 * C::KV_TILE);
+          for (int pn = 0; pn < C::PANELS; ++pn) {
+            tma_load_3d(sbase + C::OFF_K + pn * C::KV_PANEL, &p.k_map, BAR(C::B_KV), 64 * pn, I.k0, I.bh);
+            tma_load_3d(sbase + C::OFF_V + pn * C::KV_PANEL, &p.v_map, BAR(C::B_KV), 64 * pn, I.k0, I.bh);
           }
+          ++nkv;
+          if (has_next)
+            for (int pn = 0; pn < C::PANELS; ++pn) {
+              tma_prefetch_l2_3d(&p.k_map, 64 * pn, J.k0, J.bh);
+              tma_prefetch_l2_3d(&p.v_map, 64 * pn, J.k0, J.bh);
+            }
+          for (; ok && i < I.n; ++i) ok = issue_stage(i);
         }
-        wait_drain_bwd(BAR(C::B_KV), 0);
-        for (int i = max(0, it - QS); i < it; ++i) wait_drain_bwd(BAR(C::B_QDFULL + i % QS), (i / QS) & 1);
+        if (nkv > 0) wait_drain_bwd(BAR(C::B_KV), (nkv - 1) & 1);
+        for (int j = max(0, it - QS); j < it; ++j) wait_drain_bwd(BAR(C::B_QDFULL + j % QS), (j / QS) & 1);
       }
       __syncwarp();
     } else if (warp == 1 || (C::EARLY && warp == 2)) {
@@ -329,6 +381,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
       // warp 2 issues dV, dK and dQ.  The two streams touch disjoint TMEM columns
       // and are ordered only through the compute warps' barriers, so a thread
       // blocked on a commit or a wait no longer leaves the tensor pipe idle.
+      // Each issuing thread commits to KVEMPTY after its last MMA of an item
+      // that reads K or V.
       if (lane == 0) {
         constexpr uint32_t idS = make_idesc(128, BM, false, false);
         constexpr uint32_t idAcc = make_idesc(128, DH, false, true);
@@ -344,7 +398,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
                    desc_kmajor(stage_do(s), C::QD_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
           mma_commit(BAR(C::B_SDP));
         };
-        auto issue_acc = [&](int s, bool first) {
+        auto issue_acc = [&](int s, int h, bool first) {
           const uint32_t dob = stage_do(s) + h * (DH / 64) * C::QD_PANEL;
           const uint32_t qb = stage_q(s) + h * (DH / 64) * C::QD_PANEL;
 #pragma unroll
@@ -373,66 +427,108 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           }
           mma_commit(BAR(C::B_DQFULL));
         };
-        bool ok = wait_one(BAR(C::B_KV), 0, ab, (kKBwdKV << 8) | 2);
-        if (ok && n > 0 && (!C::EARLY || warp == 1)) {
-          ok = wait_one(BAR(C::B_QDFULL + 0), 0, ab, (kKBwdKV << 8) | 3);
-          if (ok) {
-            tc_fence_after();
-            issue_sdp(0);
-          }
-        }
-        if (C::EARLY && warp == 1) {
-          // S^T(i+1), dP^T(i+1) as soon as the compute warps hold S^T(i), dP^T(i) in registers.
-          for (int i = 0; ok && i + 1 < n; ++i) {
-            const int s1 = (i + 1) % QS;
-            if (!wait_one(BAR(C::B_SCONS), i & 1, ab, (kKBwdKV << 8) | 14) ||
-                !wait_one(BAR(C::B_QDFULL + s1), ((i + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_sdp(s1);
-          }
-        }
-        for (int i = 0; ok && i < n && (!C::EARLY || warp == 2); ++i) {
-          const int s = i % QS;
-          if (!wait_one(BAR(C::B_PDS), i & 1, ab, (kKBwdKV << 8) | 4)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if constexpr (C::SEP && !C::EARLY) {
-            if (i + 1 < n) {
-              const int s1 = (i + 1) % QS;
-              if (!wait_one(BAR(C::B_QDFULL + s1), ((i + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
-                ok = false;
-                break;
-              }
-              tc_fence_after();
-              issue_sdp(s1);
-            }
-          }
-          issue_acc(s, i == 0);
+        // dV, dK (and dQ) of query tile g (stage s), then the commits that free
+        // the stage and tell the compute warps P^T / dS^T have been read.
+        auto issue_tail = [&](int g, int s, int h, bool first) -> bool {
+          issue_acc(s, h, first);
           if constexpr (C::DQ) {
-            if (i > 0 && !wait_one(BAR(C::B_DQFREE), (i - 1) & 1, ab, (kKBwdKV << 8) | 6)) {
-              ok = false;
-              break;
-            }
+            if (g > 0 && !wait_one(BAR(C::B_DQFREE), (g - 1) & 1, ab, (kKBwdKV << 8) | 6)) return false;
             tc_fence_after();
             issue_dq();
           }
           mma_commit(BAR(C::B_MMA));
           mma_commit(BAR(C::B_QDEMPTY + s));
-          if constexpr (!C::SEP) {
-            if (i + 1 < n) {
-              const int s1 = (i + 1) % QS;
-              if (!wait_one(BAR(C::B_QDFULL + s1), ((i + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
+          return true;
+        };
+        bool ok = true;
+        int g = 0, nkv = 0;
+        if (C::EARLY && warp == 1) {
+          // S^T(g), dP^T(g) as soon as the compute warps hold S^T(g-1), dP^T(g-1) in registers.
+          for (int r = 0; ok; ++r) {
+            const int w = item_of(r);
+            if (w >= p.items) break;
+            const int n = coords(w).n;
+            if (n <= 0) continue;
+            if (!wait_one(BAR(C::B_KV), nkv & 1, ab, (kKBwdKV << 8) | 2)) break;
+            for (int i = 0; i < n; ++i, ++g) {
+              const int s = g % QS;
+              if ((g > 0 && !wait_one(BAR(C::B_SCONS), (g - 1) & 1, ab, (kKBwdKV << 8) | 14)) ||
+                  !wait_one(BAR(C::B_QDFULL + s), (g / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              issue_sdp(s1);
+              issue_sdp(s);
             }
+            if (!ok) break;
+            mma_commit(BAR(C::B_KVEMPTY));
+            ++nkv;
+          }
+        } else if (C::EARLY) {
+          for (int r = 0; ok; ++r) {
+            const int w = item_of(r);
+            if (w >= p.items) break;
+            const Item I = coords(w);
+            if (I.n <= 0) continue;
+            for (int i = 0; i < I.n; ++i, ++g) {
+              const int s = g % QS;
+              if (!wait_one(BAR(C::B_PDS), g & 1, ab, (kKBwdKV << 8) | 4)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              if (!issue_tail(g, s, I.h, i == 0)) {
+                ok = false;
+                break;
+              }
+            }
+            if (!ok) break;
+            mma_commit(BAR(C::B_KVEMPTY));
+          }
+        } else {
+          for (int r = 0; ok; ++r) {
+            const int w = item_of(r);
+            if (w >= p.items) break;
+            const Item I = coords(w);
+            if (I.n <= 0) continue;
+            if (!wait_one(BAR(C::B_KV), nkv & 1, ab, (kKBwdKV << 8) | 2) ||
+                !wait_one(BAR(C::B_QDFULL + g % QS), (g / QS) & 1, ab, (kKBwdKV << 8) | 3))
+              break;
+            tc_fence_after();
+            issue_sdp(g % QS);
+            for (int i = 0; i < I.n; ++i, ++g) {
+              const int s = g % QS;
+              const int s1 = (g + 1) % QS;
+              if (!wait_one(BAR(C::B_PDS), g & 1, ab, (kKBwdKV << 8) | 4)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              // SEP: S^T / dP^T of the next query tile go ahead of dV, dK, dQ.
+              if (C::SEP && i + 1 < I.n) {
+                if (!wait_one(BAR(C::B_QDFULL + s1), ((g + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                issue_sdp(s1);
+              }
+              if (!issue_tail(g, s, I.h, i == 0)) {
+                ok = false;
+                break;
+              }
+              if (!C::SEP && i + 1 < I.n) {
+                if (!wait_one(BAR(C::B_QDFULL + s1), ((g + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                issue_sdp(s1);
+              }
+            }
+            if (!ok) break;
+            mma_commit(BAR(C::B_KVEMPTY));
+            ++nkv;
           }
         }
         mma_commit(BAR(C::B_DONE));
@@ -447,203 +543,275 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
       const int c_lo = cw * C::CW;
       const int quad = warp & 3;
       const int r = quad * 32 + lane;
-      const int kj = k0 + r;
-      const bool key_ok = kj < p.N;
       const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
       const float cs = p.scale_log2;
+      uint8_t* ds_row = gbase + C::OFF_DS + r * 128;
       bool ok = true;
-      for (int i = 0; i < n; ++i) {
-        const int s = i % QS;
-        const int q0 = (qt0 + i) * BM;
-        if (!wait_warp(BAR(C::B_SDP), i & 1, ab, (kKBwdKV << 8) | 7) ||
-            !wait_warp(BAR(C::B_QDFULL + s), (i / QS) & 1, ab, (kKBwdKV << 8) | 8)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float* L = reinterpret_cast<const float*>(gbase + (stage_lse(s) - sbase));
-        const float* Dd = reinterpret_cast<const float*>(gbase + (stage_dd(s) - sbase));
-        const int lim = p.causal ? kj - q0 : -1;  // columns c < lim are masked (query < key)
-        uint8_t* ds_row = gbase + C::OFF_DS + r * 128;
-        // Writes one 32-column chunk of P^T and dS^T (packed bf16) to TMEM and,
-        // for the 5-GEMM variant, dS^T row r into the [128 keys][BM queries]
-        // swizzled shared-memory tile read by the dQ MMA.
-        auto store_chunk = [&](int c0, const uint32_t* pp, const uint32_t* pd) {
-          tmem_st_32x32b_x16(trow + C::T_PT + (c0 >> 1), pp);
-          tmem_st_32x32b_x16(trow + C::T_DST + (c0 >> 1), pd);
-          if constexpr (C::DQ) {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int ch = (c0 >> 3) + u;
-              const int pn = ch >> 3, cc = ch & 7;
-              *reinterpret_cast<uint4*>(ds_row + pn * C::DS_PANEL + ((cc ^ (r & 7)) << 4)) =
-                  make_uint4(pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
+      int g = 0;
+      for (int rr = 0; ok; ++rr) {
+        const int w = item_of(rr);
+        if (w >= p.items) break;
+        const Item I = coords(w);
+        const int kj = I.k0 + r;
+        const bool key_ok = kj < p.N;
+        if (I.n <= 0) {
+          // No query can see this key tile: zero gradients.
+          if (key_ok && cw == 0)
+            for (int c = 0; c < DH; c += 8) {
+              *reinterpret_cast<uint4*>(p.dv + ((size_t)I.bh * p.N + kj) * D + I.h * DH + c) = make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(p.dk + ((size_t)I.bh * p.N + kj) * D + I.h * DH + c) = make_uint4(0, 0, 0, 0);
             }
-          }
-        };
-        constexpr int HOLD = C::SEP ? C::CW / 2 : 16;
-        uint32_t pk_p[HOLD], pk_ds[HOLD];
-        // P^T = exp2(S^T c - lse2), dS^T = P^T (dP^T - D) for columns [c0, c0 + 32).
-        const float2 c2 = make_float2(cs, cs);
-        auto compute_chunk = [&](int c0, const uint32_t* sr, const uint32_t* dr, int hb) {
-          // Masks only in chunks that reach past the last key or below the diagonal.
-          const bool masked = !key_ok || lim > c0;
-#pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            const float4 l4 = *reinterpret_cast<const float4*>(L + c0 + e);
-            const float4 d4 = *reinterpret_cast<const float4*>(Dd + c0 + e);
-            const float2 x01 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
-                                     make_float2(l4.x, l4.y));
-            const float2 x23 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2,
-                                     make_float2(l4.z, l4.w));
-            float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
-            float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
-            if (masked) {
-              const int c = c0 + e;
-              if (!key_ok || c < lim) p01.x = 0.f;
-              if (!key_ok || c + 1 < lim) p01.y = 0.f;
-              if (!key_ok || c + 2 < lim) p23.x = 0.f;
-              if (!key_ok || c + 3 < lim) p23.y = 0.f;
-            }
-            const float2 d01 = fmul2(p01, fadd2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
-                                                make_float2(d4.x, d4.y)));
-            const float2 d23 = fmul2(p23, fadd2(make_float2(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
-                                                make_float2(d4.z, d4.w)));
-            pk_p[hb + (e >> 1)] = pack_bf16(p01.x, p01.y);
-            pk_p[hb + (e >> 1) + 1] = pack_bf16(p23.x, p23.y);
-            pk_ds[hb + (e >> 1)] = pack_bf16(d01.x, d01.y);
-            pk_ds[hb + (e >> 1) + 1] = pack_bf16(d23.x, d23.y);
-          }
-        };
-        if constexpr (C::EARLY) {
-          uint32_t sr[C::CW], dr[C::CW];
-#pragma unroll
-          for (int c0 = 0; c0 < C::CW; c0 += 32) {
-            tmem_ld_32x32b_x32(trow + C::T_ST + c_lo + c0, sr + c0);
-            tmem_ld_32x32b_x32(trow + C::T_DPT + c_lo + c0, dr + c0);
-          }
-          tmem_wait_ld();
-          reg_fence<C::CW>(sr);
-          reg_fence<C::CW>(dr);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(C::B_SCONS));
-#pragma unroll
-          for (int c0 = 0; c0 < C::CW; c0 += 32) compute_chunk(c_lo + c0, sr + c0, dr + c0, c0 >> 1);
-        } else {
-#pragma unroll
-          for (int c0 = 0; c0 < BM; c0 += 32) {
-            uint32_t sr[32], dr[32];
-            tmem_ld_32x32b_x32(trow + C::T_ST + c0, sr);
-            tmem_ld_32x32b_x32(trow + C::T_DPT + c0, dr);
-            tmem_wait_ld();
-            reg_fence<32>(sr);
-            reg_fence<32>(dr);
-            compute_chunk(c0, sr, dr, C::SEP ? (c0 >> 1) : 0);
-            if constexpr (!C::SEP) store_chunk(c0, pk_p, pk_ds);
-          }
+          continue;
         }
-        if constexpr (C::SEP) {
-          // dV(i-1), dK(i-1), dQ(i-1) read P^T, dS^T (TMEM) and dS^T (smem): wait for them.
-          if (i > 0 && !wait_warp(BAR(C::B_MMA), (i - 1) & 1, ab, (kKBwdKV << 8) | 9)) {
+        for (int i = 0; i < I.n; ++i, ++g) {
+          const int s = g % QS;
+          const int q0 = (I.qt0 + i) * BM;
+          if (!wait_warp(BAR(C::B_SDP), g & 1, ab, (kKBwdKV << 8) | 7) ||
+              !wait_warp(BAR(C::B_QDFULL + s), (g / QS) & 1, ab, (kKBwdKV << 8) | 8)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const float* L = reinterpret_cast<const float*>(gbase + (stage_lse(s) - sbase));
+          const float* Dd = reinterpret_cast<const float*>(gbase + (stage_dd(s) - sbase));
+          const int lim = p.causal ? kj - q0 : -1;  // columns c < lim are masked (query < key)
+          // Writes one 32-column chunk of P^T and dS^T (packed bf16) to TMEM and,
+          // for the 5-GEMM variant, dS^T row r into the [128 keys][BM queries]
+          // swizzled shared-memory tile read by the dQ MMA.
+          auto store_chunk = [&](int c0, const uint32_t* pp, const uint32_t* pd) {
+            tmem_st_32x32b_x16(trow + C::T_PT + (c0 >> 1), pp);
+            tmem_st_32x32b_x16(trow + C::T_DST + (c0 >> 1), pd);
+            if constexpr (C::DQ) {
 #pragma unroll
-          for (int c0 = 0; c0 < C::CW; c0 += 32) store_chunk(c_lo + c0, pk_p + (c0 >> 1), pk_ds + (c0 >> 1));
+              for (int u = 0; u < 4; ++u) {
+                const int ch = (c0 >> 3) + u;
+                const int pn = ch >> 3, cc = ch & 7;
+                *reinterpret_cast<uint4*>(ds_row + pn * C::DS_PANEL + ((cc ^ (r & 7)) << 4)) =
+                    make_uint4(pd[4 * u], pd[4 * u + 1], pd[4 * u + 2], pd[4 * u + 3]);
+              }
+            }
+          };
+          constexpr int HOLD = C::SEP ? C::CW / 2 : 16;
+          uint32_t pk_p[HOLD], pk_ds[HOLD];
+          // P^T = exp2(S^T c - lse2), dS^T = P^T (dP^T - D) for columns [c0, c0 + 32).
+          const float2 c2 = make_float2(cs, cs);
+          auto compute_chunk = [&](int c0, const uint32_t* sr, const uint32_t* dr, int hb) {
+            // Masks only in chunks that reach past the last key or below the diagonal.
+            const bool masked = !key_ok || lim > c0;
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const float4 l4 = *reinterpret_cast<const float4*>(L + c0 + e);
+              const float4 d4 = *reinterpret_cast<const float4*>(Dd + c0 + e);
+              const float2 x01 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2,
+                                       make_float2(l4.x, l4.y));
+              const float2 x23 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2,
+                                       make_float2(l4.z, l4.w));
+              float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+              float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+              if (masked) {
+                const int c = c0 + e;
+                if (!key_ok || c < lim) p01.x = 0.f;
+                if (!key_ok || c + 1 < lim) p01.y = 0.f;
+                if (!key_ok || c + 2 < lim) p23.x = 0.f;
+                if (!key_ok || c + 3 < lim) p23.y = 0.f;
+              }
+              const float2 d01 = fmul2(p01, fadd2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])),
+                                                  make_float2(d4.x, d4.y)));
+              const float2 d23 = fmul2(p23, fadd2(make_float2(__uint_as_float(dr[e + 2]), __uint_as_float(dr[e + 3])),
+                                                  make_float2(d4.z, d4.w)));
+              pk_p[hb + (e >> 1)] = pack_bf16(p01.x, p01.y);
+              pk_p[hb + (e >> 1) + 1] = pack_bf16(p23.x, p23.y);
+              pk_ds[hb + (e >> 1)] = pack_bf16(d01.x, d01.y);
+              pk_ds[hb + (e >> 1) + 1] = pack_bf16(d23.x, d23.y);
+            }
+          };
+          if constexpr (C::EARLY) {
+            uint32_t sr[C::CW], dr[C::CW];
+#pragma unroll
+            for (int c0 = 0; c0 < C::CW; c0 += 32) {
+              tmem_ld_32x32b_x32(trow + C::T_ST + c_lo + c0, sr + c0);
+              tmem_ld_32x32b_x32(trow + C::T_DPT + c_lo + c0, dr + c0);
+            }
+            tmem_wait_ld();
+            reg_fence<C::CW>(sr);
+            reg_fence<C::CW>(dr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(C::B_SCONS));
+#pragma unroll
+            for (int c0 = 0; c0 < C::CW; c0 += 32) compute_chunk(c_lo + c0, sr + c0, dr + c0, c0 >> 1);
+          } else {
+#pragma unroll
+            for (int c0 = 0; c0 < BM; c0 += 32) {
+              uint32_t sr[32], dr[32];
+              tmem_ld_32x32b_x32(trow + C::T_ST + c0, sr);
+              tmem_ld_32x32b_x32(trow + C::T_DPT + c0, dr);
+              tmem_wait_ld();
+              reg_fence<32>(sr);
+              reg_fence<32>(dr);
+              compute_chunk(c0, sr, dr, C::SEP ? (c0 >> 1) : 0);
+              if constexpr (!C::SEP) store_chunk(c0, pk_p, pk_ds);
+            }
+          }
+          if constexpr (C::SEP) {
+            // dV, dK, dQ of the previous query tile read P^T, dS^T (TMEM) and dS^T (smem): wait for them.
+            if (g > 0 && !wait_warp(BAR(C::B_MMA), (g - 1) & 1, ab, (kKBwdKV << 8) | 9)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c0 = 0; c0 < C::CW; c0 += 32) store_chunk(c_lo + c0, pk_p + (c0 >> 1), pk_ds + (c0 >> 1));
+          }
+          if constexpr (C::DQ) fence_proxy_async_smem();
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(C::B_PDS));
         }
-        if constexpr (C::DQ) fence_proxy_async_smem();
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(C::B_PDS));
-      }
-      // ------------------------------------------------ dV, dK epilogue
-      if (ok && n > 0 && wait_warp(BAR(C::B_MMA), (n - 1) & 1, ab, (kKBwdKV << 8) | 10)) {
+        if (!ok) break;
+        // ------------------------------------------------ dV, dK epilogue
+        // The TMEM reads finish before these warps arrive on PDS for the next
+        // item's first query tile, whose dV / dK MMAs overwrite the accumulators.
+        if (!wait_warp(BAR(C::B_MMA), (g - 1) & 1, ab, (kKBwdKV << 8) | 10)) break;
         tc_fence_after();
-        const bool store = key_ok;
-        const size_t rowoff = ((size_t)bh * p.N + (size_t)(store ? kj : 0)) * D + h * DH;
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           if (C::NCW == 2 && which != cw) continue;  // two warpgroups: one stores dV, the other dK
-          uint16_t* dst = (which == 0 ? p.dv : p.dk) + rowoff;
+          uint16_t* dst = (which == 0 ? p.dv : p.dk) + (size_t)I.bh * p.N * D + I.h * DH;
           const float mul = which == 0 ? 1.f : p.scale;
           const uint32_t tacc = trow + (which == 0 ? C::T_DV : C::T_DK);
+          if constexpr (C::DQ) {
+            // Staged through this warp's own footprint of the dS^T tile (free once
+            // the last dQ MMA has read it): each thread writes its row, then the warp
+            // writes R consecutive 16-byte chunks of 32 / R rows per instruction, so a
+            // warp store covers a few contiguous row segments instead of 32 rows.
+            constexpr int EW = C::CW < DH ? C::CW : DH;  // columns per round
+            constexpr int R = EW / 8;                    // 16-byte chunks per row per round
+            static_assert(EW % 32 == 0 && 32 % R == 0, "epilogue staging shape");
+            auto ds_chunk = [&](int rr, int u) -> uint4* {
+              const int ch = (c_lo >> 3) + u;
+              return reinterpret_cast<uint4*>(gbase + C::OFF_DS + (ch >> 3) * C::DS_PANEL + rr * 128 +
+                                              (((ch & 7) ^ (rr & 7)) << 4));
+            };
 #pragma unroll
-          for (int c0 = 0; c0 < DH; c0 += 32) {
-            uint32_t rr[32];
-            tmem_ld_32x32b_x32(tacc + c0, rr);
-            tmem_wait_ld();
-            reg_fence<32>(rr);
-            uint32_t pk[16];
+            for (int c0 = 0; c0 < DH; c0 += EW) {
+              uint32_t pk[EW / 2];
 #pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              pk[e >> 1] = pack_bf16(__uint_as_float(rr[e]) * mul, __uint_as_float(rr[e + 1]) * mul);
-            if (store) {
-              uint4* o4 = reinterpret_cast<uint4*>(dst + c0);
+              for (int cc = 0; cc < EW; cc += 32) {
+                uint32_t rv[32];
+                tmem_ld_32x32b_x32(tacc + c0 + cc, rv);
+                tmem_wait_ld();
+                reg_fence<32>(rv);
 #pragma unroll
-              for (int v = 0; v < 4; ++v) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                for (int e = 0; e < 32; e += 2)
+                  pk[(cc + e) >> 1] = pack_bf16(__uint_as_float(rv[e]) * mul, __uint_as_float(rv[e + 1]) * mul);
+              }
+#pragma unroll
+              for (int u = 0; u < R; ++u) *ds_chunk(r, u) = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < R; ++j) {
+                const int rr = quad * 32 + j * (32 / R) + lane / R;
+                const int u = lane % R;
+                const uint4 val = *ds_chunk(rr, u);
+                if (I.k0 + rr < p.N) *reinterpret_cast<uint4*>(dst + (size_t)(I.k0 + rr) * D + c0 + 8 * u) = val;
+              }
+              __syncwarp();
+            }
+          } else {
+            uint16_t* drow = dst + (size_t)(key_ok ? kj : 0) * D;
+#pragma unroll
+            for (int c0 = 0; c0 < DH; c0 += 32) {
+              uint32_t rv[32];
+              tmem_ld_32x32b_x32(tacc + c0, rv);
+              tmem_wait_ld();
+              reg_fence<32>(rv);
+              uint32_t pk[16];
+#pragma unroll
+              for (int e = 0; e < 32; e += 2)
+                pk[e >> 1] = pack_bf16(__uint_as_float(rv[e]) * mul, __uint_as_float(rv[e + 1]) * mul);
+              if (key_ok) {
+                uint4* o4 = reinterpret_cast<uint4*>(drow + c0);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+              }
             }
           }
         }
-      } else if (n == 0 && key_ok && cw == 0) {
-        // No query can see this key (possible only with ragged tails): zero gradients.
-        for (int c = 0; c < DH; c += 8) {
-          *reinterpret_cast<uint4*>(p.dv + ((size_t)bh * p.N + kj) * D + h * DH + c) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(p.dk + ((size_t)bh * p.N + kj) * D + h * DH + c) = make_uint4(0, 0, 0, 0);
-        }
+        tc_fence_before();
       }
     } else {
       if constexpr (C::DQ) {
       // ------------------------------------------------------ dQ drain (5-GEMM)
+      if constexpr (kSplitRegs && C::REG_DRAIN < C::REG_LAUNCH) regs_shrink<C::REG_DRAIN>();
       const int quad = warp & 3;
       const int lr = quad * 32 + lane;  // TMEM lane: d index (dQ^T) or query row (dQ)
       const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16) + C::T_DQ;
       float* stg = reinterpret_cast<float*>(gbase + C::OFF_STG);
       const bool leader = (warp == C::DRAIN_W0 && lane == 0);
-      for (int i = 0; i < n; ++i) {
-        if (!wait_warp(BAR(C::B_DQFULL), i & 1, ab, (kKBwdKV << 8) | 11)) break;
-        tc_fence_after();
-        constexpr int COLS = C::DQ_COLS;
-        uint32_t v[COLS];
+      bool ok = true;
+      int g = 0;
+      for (int rr = 0; ok; ++rr) {
+        const int w = item_of(rr);
+        if (w >= p.items) break;
+        const Item I = coords(w);
+        for (int i = 0; i < I.n; ++i, ++g) {
+          if (!wait_warp(BAR(C::B_DQFULL), g & 1, ab, (kKBwdKV << 8) | 11)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          constexpr int COLS = C::DQ_COLS;
+          uint32_t v[COLS];
 #pragma unroll
-        for (int c0 = 0; c0 < COLS; c0 += 32) tmem_ld_32x32b_x32(trow + c0, v + c0);
-        tmem_wait_ld();
-        reg_fence<COLS>(v);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(C::B_DQFREE));
-        if constexpr (C::DQ_T) {
-          // lanes = d index lr, columns = query q of the tile: for each q the warp
-          // adds 32 consecutive floats of accumulator row q (one 128-byte line).
-          float* rows = p.dqacc + ((size_t)bh * p.Npad + (size_t)(qt0 + i) * BM) * D;
+          for (int c0 = 0; c0 < COLS; c0 += 32) tmem_ld_32x32b_x32(trow + c0, v + c0);
+          tmem_wait_ld();
+          reg_fence<COLS>(v);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(C::B_DQFREE));
+          const int q0 = (I.qt0 + i) * BM;
+          if constexpr (C::DQ_T) {
+            // lanes = d index lr, columns = query q of the tile: for each q the warp
+            // adds 32 consecutive floats of accumulator row q (one 128-byte line).
+            float* rows = p.dqacc + ((size_t)I.bh * p.Npad + (size_t)q0) * D;
 #pragma unroll
-          for (int q = 0; q < COLS; ++q) red_add_f32(rows + q * D + dq_swz(q, lr), __uint_as_float(v[q]));
-          continue;
-        }
-        // The previous bulk reduction must have finished reading the staging tile.
-        if (leader) {
-          bulk_wait_read0();
-          mbar_arrive(BAR(C::B_STGFREE));
-        }
-        if (!wait_warp(BAR(C::B_STGFREE), i & 1, ab, (kKBwdKV << 8) | 12)) break;
-        {
-          // lanes = query row lr, columns = d
+            for (int q = 0; q < COLS; ++q) red_add_f32(rows + q * D + dq_swz(q, lr), __uint_as_float(v[q]));
+            continue;
+          }
+          // The previous bulk reduction must have finished reading the staging tile.
+          if (leader) {
+            bulk_wait_read0();
+            mbar_arrive(BAR(C::B_STGFREE));
+          }
+          if (!wait_warp(BAR(C::B_STGFREE), g & 1, ab, (kKBwdKV << 8) | 12)) {
+            ok = false;
+            break;
+          }
+          {
+            // lanes = query row lr, columns = d
 #pragma unroll
-          for (int c = 0; c < COLS; c += 4)
-            *reinterpret_cast<float4*>(stg + lr * D + dq_swz(lr, c)) =
-                make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]), __uint_as_float(v[c + 2]),
-                            __uint_as_float(v[c + 3]));
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(C::B_STGFULL));
-        if (leader) {
-          if (!wait_one(BAR(C::B_STGFULL), i & 1, ab, (kKBwdKV << 8) | 13)) break;
-          const int q0 = (qt0 + i) * BM;
-          bulk_reduce_add_f32(p.dqacc + ((size_t)bh * p.Npad + q0) * D, smem_u32(stg), C::STG_BYTES);
-          bulk_commit();
+            for (int c = 0; c < COLS; c += 4)
+              *reinterpret_cast<float4*>(stg + lr * D + dq_swz(lr, c)) =
+                  make_float4(__uint_as_float(v[c]), __uint_as_float(v[c + 1]), __uint_as_float(v[c + 2]),
+                              __uint_as_float(v[c + 3]));
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(C::B_STGFULL));
+          bool lok = true;
+          if (leader) {
+            lok = wait_one(BAR(C::B_STGFULL), g & 1, ab, (kKBwdKV << 8) | 13);
+            if (lok) {
+              bulk_reduce_add_f32(p.dqacc + ((size_t)I.bh * p.Npad + q0) * D, smem_u32(stg), C::STG_BYTES);
+              bulk_commit();
+            }
+          }
+          if (!__all_sync(0xffffffffu, lok)) {  // the whole warp leaves together
+            ok = false;
+            break;
+          }
         }
       }
       if (leader) bulk_wait0();

@@ -104,8 +104,11 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   kp.scale = scale;
   kp.causal = causal;
   kp.group = causal ? BH : head_group(((N + KV::BN - 1) / KV::BN) * KV::DSPLIT, BH);
-  const long long kv_blocks = (long long)((N + KV::BN - 1) / KV::BN) * BH * KV::DSPLIT;
-  if ((s = launch(KV::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<KV>, dim3((unsigned)kv_blocks),
+  const long long kv_items = (long long)((N + KV::BN - 1) / KV::BN) * BH * KV::DSPLIT;
+  if (kv_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  kp.items = (int)kv_items;
+  const long long kv_grid = std::min<long long>(kv_items, sm_count_cached());
+  if ((s = launch(KV::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<KV>, dim3((unsigned)kv_grid),
                   dim3(KV::THREADS), KV::SMEM_BYTES, st, kp)) != FA_OK)
     return s;
 
