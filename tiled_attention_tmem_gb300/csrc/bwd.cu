@@ -25,6 +25,7 @@ struct Workspace {
   float* lse2;
   float* dd;
   float* dqacc;
+  int* sched;  // work-item counters, in the workspace's last 256 bytes
 };
 
 Workspace carve(void* ws, int BH, int Npad, int d, bool with_dq) {
@@ -34,7 +35,7 @@ Workspace carve(void* ws, int BH, int Npad, int d, bool with_dq) {
   w.lse2 = reinterpret_cast<float*>(b);
   w.dd = reinterpret_cast<float*>(b + align256(4 * rows));
   w.dqacc = with_dq ? reinterpret_cast<float*>(b + 2 * align256(4 * rows)) : nullptr;
-  (void)d;
+  w.sched = reinterpret_cast<int*>(b + 2 * align256(4 * rows) + (with_dq ? 4 * rows * (size_t)d : 0));
   return w;
 }
 
@@ -48,7 +49,7 @@ template <int D>
 fa_status run_pre(const void* o, const void* dO, const float* lse, const Workspace& w, int BH, int N, int Npad,
                   cudaStream_t st) {
   PreParams p{static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, w.lse2, w.dd, w.dqacc,
-              N, Npad, BH, D};
+              N, Npad, BH, D, w.sched};
   const long long threads = (long long)BH * Npad * (D / 8);
   const long long blocks = std::min<long long>((threads + 255) / 256, (long long)sm_count() * 8);
   prof_before(FA_KERNEL_BWD_PRE, st);
@@ -94,7 +95,8 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
-  p.group = causal ? BH : head_group(((N + C::BN - 1) / C::BN) * C::DSPLIT, BH);
+  p.group = causal ? l2_head_group(N, C::D, BH) : head_group(((N + C::BN - 1) / C::BN) * C::DSPLIT, BH);
+  p.sched = w.sched;
   const long long items = (long long)((N + C::BN - 1) / C::BN) * BH * C::DSPLIT;
   if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.items = (int)items;

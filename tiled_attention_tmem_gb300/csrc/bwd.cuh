@@ -56,6 +56,7 @@ struct PreParams {
   float* dd;
   float* dqacc;  // nullptr for the 7-GEMM variant
   int N, Npad, BH, d;
+  int* sched;    // work-item counters of the following kernels, zeroed here
 };
 
 template <int D>
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
       p.dd[row] = -acc;
       p.lse2[row] = i < p.N ? -(p.lse[(size_t)bh * p.N + i] * kLog2e) : -INFINITY;
     }
+    if (p.sched && row == 0 && sub < 4) p.sched[sub] = 0;
     if (p.dqacc) {
       float4* z = reinterpret_cast<float4*>(p.dqacc + (size_t)row * D + sub * 8);
       z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -154,6 +156,7 @@ struct BwdKVParams {
   int causal;
   int group;  // heads per launch-order group
   int items;  // work items (key tiles x d parts x heads); the grid is persistent over them
+  int* sched; // next unclaimed work item (zero at launch)
 };
 
 template <int D_, int BM_, bool DQ_, int DSPLIT_, int QS_, bool SEP_>
@@ -195,9 +198,12 @@ struct BwdKVCfg {
                        B_PDS = B_SDP + 1, B_MMA = B_PDS + 1, B_DQFULL = B_MMA + 1,
                        B_DQFREE = B_DQFULL + 1, B_STGFREE = B_DQFREE + 1, B_STGFULL = B_STGFREE + 1,
                        B_SCONS = B_STGFULL + 1, B_DONE = B_SCONS + 1, B_KVEMPTY = B_DONE + 1,
-                       NBAR = B_KVEMPTY + 1;
+                       B_ITEMFULL = B_KVEMPTY + 1, B_ITEMEMPTY = B_ITEMFULL + 4, NBAR = B_ITEMEMPTY + 4;
+  static constexpr int IQ = 4;  // claimed work items passed from the producer to the other roles
+  // Roles that read each work item: the MMA issuing thread(s), the compute warps, the drain warps.
+  static constexpr int ITEM_READERS = (EARLY ? 2 : 1) + 4 * NCW + (DQ ? 4 : 0);
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 32 + 1024;
   // TMEM columns
   static constexpr int T_ST = 0, T_DPT = BM;
   static constexpr int T_PT = SEP ? 2 * BM : T_ST;
@@ -243,6 +249,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
     *abort_flag = (*reinterpret_cast<volatile int*>(p.err) != 0) ? 1 : 0;
     mbar_init(BAR(C::B_KV), 1);
     mbar_init(BAR(C::B_KVEMPTY), C::EARLY ? 2 : 1);
+    for (int k = 0; k < C::IQ; ++k) {
+      mbar_init(BAR(C::B_ITEMFULL + k), 1);
+      mbar_init(BAR(C::B_ITEMEMPTY + k), C::ITEM_READERS);
+    }
     for (int s = 0; s < QS; ++s) {
       mbar_init(BAR(C::B_QDFULL + s), 1);
       mbar_init(BAR(C::B_QDEMPTY + s), 1);
@@ -269,16 +279,33 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
   const CtaAbort ab{abort_flag, p.err};
 
   // Persistent work loop.  Work item w = (key tile, d part, head) in launch
-  // order: under the causal mask the key tiles that the most query tiles see
-  // come first, heads varying fastest; without it heads are grouped for L2
-  // reuse.  CTA c takes items in snake order over rounds (c, 2G-1-c, 2G+c, ...)
-  // so heavy and light items even out.  Every role walks the same items and
-  // counts the same query tiles, so barrier phases run on across items.
+  // order: heads in groups for L2 reuse of their Q, dO and dQ accumulator,
+  // and inside a group the key tiles that the most query tiles see first
+  // (under the causal mask), heads varying fastest.  The producer claims items
+  // from a global counter one item ahead (so idle SMs take the next item,
+  // longest first) and passes each claimed index through a small shared-memory
+  // ring to the other roles.  Every role walks the same items and counts the
+  // same query tiles, so barrier phases run on across items.
   const int n_kt = (p.N + C::BN - 1) / C::BN;
   const int n_qt = (p.N + BM - 1) / BM;
-  auto item_of = [&](int r) -> int {
-    const int G = gridDim.x, c = blockIdx.x;
-    return r * G + ((r & 1) ? (G - 1 - c) : c);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 16);
+  // Item claimed t-th by this CTA (>= p.items once the counter ran out), or -1
+  // if the wait gave up.  Single-thread readers.
+  auto item_one = [&](int t) -> int {
+    const int k = t % C::IQ;
+    if (!wait_one(BAR(C::B_ITEMFULL + k), (t / C::IQ) & 1, ab, (kKBwdKV << 8) | 18)) return -1;
+    const int w = item_ring[k];
+    mbar_arrive(BAR(C::B_ITEMEMPTY + k));
+    return w;
+  };
+  // The same for a whole warp (lane 0 releases the slot).
+  auto item_warp = [&](int t) -> int {
+    const int k = t % C::IQ;
+    if (!wait_warp(BAR(C::B_ITEMFULL + k), (t / C::IQ) & 1, ab, (kKBwdKV << 8) | 18)) return -1;
+    const int w = item_ring[k];
+    __syncwarp();
+    if (lane_id() == 0) mbar_arrive(BAR(C::B_ITEMEMPTY + k));
+    return w;
   };
   struct Item {
     int bh, h, k0, qt0, n;  // head, d part, first key, first query tile, query tiles
@@ -299,10 +326,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
   auto stage_lse = [&](int s) { return stage_q(s) + 2 * C::QD_TILE; };
   auto stage_dd = [&](int s) { return stage_lse(s) + BM * 4; };
 
-  // 5-GEMM (384 threads, 168 registers each at launch): each role branch
-  // starts with its warpgroup's register budget.  The producer/MMA warpgroup
-  // gives registers to the compute warpgroup; 128 * (80 + 224 + 168) stays
-  // within the 384 * 168 the block was launched with.
+  // With 384 or 512 threads each role branch starts with its warpgroup's
+  // register budget (REG_LOW, REG_COMPUTE, REG_DRAIN): the producer/MMA
+  // warpgroup gives registers to the compute warpgroup(s).
   constexpr bool kSplitRegs = C::THREADS >= 384;
   if (!*abort_flag) {
     if (warp < 4) {
@@ -326,12 +352,24 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
             tma_prefetch_l2_3d(&p.do_map, 64 * pn, prow, I.bh);
           }
         };
-        for (int r = 0; ok; ++r) {
-          const int w = item_of(r);
-          if (w >= p.items) break;
+        int published = 0;
+        auto publish = [&](int w) -> bool {
+          const int k = published % C::IQ;
+          if (!wait_one(BAR(C::B_ITEMEMPTY + k), ((published / C::IQ) & 1) ^ 1, ab, (kKBwdKV << 8) | 17))
+            return false;
+          item_ring[k] = w;
+          mbar_arrive(BAR(C::B_ITEMFULL + k));
+          ++published;
+          return true;
+        };
+        int wn = atomicAdd(p.sched, 1);
+        ok = publish(wn);
+        while (ok && wn < p.items) {
+          const int w = wn;
+          wn = atomicAdd(p.sched, 1);
+          if (!publish(wn)) break;
           const Item I = coords(w);
           if (I.n <= 0) continue;
-          const int wn = item_of(r + 1);
           const bool has_next = wn < p.items;
           const Item J = has_next ? coords(wn) : I;
           auto issue_stage = [&](int i) -> bool {
@@ -445,8 +483,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         if (C::EARLY && warp == 1) {
           // S^T(g), dP^T(g) as soon as the compute warps hold S^T(g-1), dP^T(g-1) in registers.
           for (int r = 0; ok; ++r) {
-            const int w = item_of(r);
-            if (w >= p.items) break;
+            const int w = item_one(r);
+            if (w < 0 || w >= p.items) break;
             const int n = coords(w).n;
             if (n <= 0) continue;
             if (!wait_one(BAR(C::B_KV), nkv & 1, ab, (kKBwdKV << 8) | 2)) break;
@@ -466,8 +504,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           }
         } else if (C::EARLY) {
           for (int r = 0; ok; ++r) {
-            const int w = item_of(r);
-            if (w >= p.items) break;
+            const int w = item_one(r);
+            if (w < 0 || w >= p.items) break;
             const Item I = coords(w);
             if (I.n <= 0) continue;
             for (int i = 0; i < I.n; ++i, ++g) {
@@ -487,8 +525,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           }
         } else {
           for (int r = 0; ok; ++r) {
-            const int w = item_of(r);
-            if (w >= p.items) break;
+            const int w = item_one(r);
+            if (w < 0 || w >= p.items) break;
             const Item I = coords(w);
             if (I.n <= 0) continue;
             if (!wait_one(BAR(C::B_KV), nkv & 1, ab, (kKBwdKV << 8) | 2) ||
@@ -549,8 +587,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
       bool ok = true;
       int g = 0;
       for (int rr = 0; ok; ++rr) {
-        const int w = item_of(rr);
-        if (w >= p.items) break;
+        const int w = item_warp(rr);
+        if (w < 0 || w >= p.items) break;
         const Item I = coords(w);
         const int kj = I.k0 + r;
         const bool key_ok = kj < p.N;
@@ -753,8 +791,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
       bool ok = true;
       int g = 0;
       for (int rr = 0; ok; ++rr) {
-        const int w = item_of(rr);
-        if (w >= p.items) break;
+        const int w = item_warp(rr);
+        if (w < 0 || w >= p.items) break;
         const Item I = coords(w);
         for (int i = 0; i < I.n; ++i, ++g) {
           if (!wait_warp(BAR(C::B_DQFULL), g & 1, ab, (kKBwdKV << 8) | 11)) {

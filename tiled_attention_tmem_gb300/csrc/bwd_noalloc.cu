@@ -70,6 +70,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
               unsigned char* base, cudaStream_t st) {
   const int Npad = (N + 127) / 128 * 128;
   int* err = reinterpret_cast<int*>(base);
+  int* sched = reinterpret_cast<int*>(base + 64);  // work-item counters, zeroed by the preprocess kernel
   unsigned char* ws = base + kErrSlot;
   float* lse2 = reinterpret_cast<float*>(ws);
   float* dd = reinterpret_cast<float*>(ws + a256(4 * (size_t)BH * Npad));
@@ -78,7 +79,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   if (e != cudaSuccess) return record_cuda_error(e);
 
   PreParams pp{static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, lse2, dd, dqacc, N, Npad,
-               BH, D};
+               BH, D, sched};
   const long long pre_threads = (long long)BH * Npad * (D / 8);
   bwd_pre_kernel<D><<<(unsigned)std::min<long long>((pre_threads + 255) / 256, (long long)sms() * 8), 256, 0, st>>>(pp);
   if ((e = cudaGetLastError()) != cudaSuccess) return record_cuda_error(e);
@@ -103,7 +104,8 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   kp.scale_log2 = scale * kLog2e;
   kp.scale = scale;
   kp.causal = causal;
-  kp.group = causal ? BH : head_group(((N + KV::BN - 1) / KV::BN) * KV::DSPLIT, BH);
+  kp.group = causal ? l2_head_group(N, D, BH) : head_group(((N + KV::BN - 1) / KV::BN) * KV::DSPLIT, BH);
+  kp.sched = sched;
   const long long kv_items = (long long)((N + KV::BN - 1) / KV::BN) * BH * KV::DSPLIT;
   if (kv_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   kp.items = (int)kv_items;

@@ -85,6 +85,17 @@ int head_group(int tiles_per_head, int BH) {
   return g < 1 ? 1 : (g > BH ? BH : g);
 }
 
+int l2_head_group(int N, int d, int BH) {
+  // Q, K, V, dO (bf16) and the fp32 dQ accumulator of one head; about 96 MiB
+  // of them in flight stays well inside L2 next to the other traffic.
+  const double per_head = 12.0 * (double)N * (double)d;
+  const double g = per_head > 0 ? (96.0 * 1024 * 1024) / per_head : (double)BH;
+  const int gi = g < 1.0 ? 1 : (g > (double)BH ? BH : (int)g);
+  // Equal-sized groups: a small last group would start its heaviest items last.
+  const int ngroups = (BH + gi - 1) / gi;
+  return (BH + ngroups - 1) / ngroups;
+}
+
 fa_status record_cuda_error(cudaError_t e) {
   g_last_cuda_error = (int)e;
   return FA_ERR_LAUNCH;

@@ -21,10 +21,14 @@ fa_status make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType 
                         CUtensorMapSwizzle swizzle);
 
 // Heads per launch-order group: enough heads for about two waves of blocks on
-// this device (at least 1, at most BH).  Launchers use one group of all heads
-// under the causal mask, where heaviest-tile-first across every head balances
-// better than locality helps.
+// this device (at least 1, at most BH).  The statically scheduled kernels use
+// one group of all heads under the causal mask, where heaviest-tile-first
+// across every head balances better than locality helps.
 int head_group(int tiles_per_head, int BH);
+// Heads per launch-order group so that their backward operands (Q, K, V, dO
+// and the fp32 dQ accumulator) fit in L2; for kernels that claim work items
+// dynamically, which keeps the balance of heaviest-first inside each group.
+int l2_head_group(int N, int d, int BH);
 
 // Multiprocessor count of the current device (cached per device).
 int sm_count_cached();
