@@ -105,19 +105,32 @@ struct ConvParams {
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_conv_kernel(const ConvParams p) {
-  const long long n4 = (long long)p.BH * p.N * D / 4;  // groups of 4 output columns
-  for (long long g = (long long)blockIdx.x * 256 + threadIdx.x; g < n4; g += (long long)gridDim.x * 256) {
-    const long long e = g * 4;
+  // Each thread converts 8 consecutive columns (two 16-byte loads, one 16-byte
+  // store); two groups per iteration keep four loads in flight.
+  const long long n8 = (long long)p.BH * p.N * D / 8;
+  const long long stride = (long long)gridDim.x * 256;
+  auto convert = [&](long long g) {
+    const long long e = g * 8;
     const int c = (int)(e % D);
     const long long rowg = e / D;  // bh * N + i
     const int bh = (int)(rowg / p.N);
     const int i = (int)(rowg % p.N);
-    const float4 v = *reinterpret_cast<const float4*>(p.dqacc + ((size_t)bh * p.Npad + i) * D + dq_swz(i, c));
-    uint2 out;
-    out.x = pack_bf16(v.x * p.scale, v.y * p.scale);
-    out.y = pack_bf16(v.z * p.scale, v.w * p.scale);
-    *reinterpret_cast<uint2*>(p.dq + e) = out;
+    const float* row = p.dqacc + ((size_t)bh * p.Npad + i) * D;
+    const float4 a = *reinterpret_cast<const float4*>(row + dq_swz(i, c));
+    const float4 b = *reinterpret_cast<const float4*>(row + dq_swz(i, c + 4));
+    uint4 out;
+    out.x = pack_bf16(a.x * p.scale, a.y * p.scale);
+    out.y = pack_bf16(a.z * p.scale, a.w * p.scale);
+    out.z = pack_bf16(b.x * p.scale, b.y * p.scale);
+    out.w = pack_bf16(b.z * p.scale, b.w * p.scale);
+    *reinterpret_cast<uint4*>(p.dq + e) = out;
+  };
+  long long g = (long long)blockIdx.x * 256 + threadIdx.x;
+  for (; g + stride < n8; g += 2 * stride) {
+    convert(g);
+    convert(g + stride);
   }
+  if (g < n8) convert(g);
 }
 
 // ------------------------------------------------------------ dK/dV kernel
@@ -190,9 +203,8 @@ struct BwdKVCfg {
   static constexpr uint32_t OFF_STAGE = OFF_V + KV_TILE;  // Q, dO, lse2, dd per stage
   static constexpr uint32_t OFF_DS = OFF_STAGE + QS * STAGE_BYTES;
   static constexpr uint32_t OFF_STG = OFF_DS + (DQ ? DS_TILE : 0);
-  // Shared-memory staging for bulk dQ reductions (dQ orientation only; dQ^T is
-  // reduced straight from registers).
-  static constexpr uint32_t STG_BYTES = (DQ && !DQ_T) ? BM * D * 4 : 0;
+  // Shared-memory staging for the bulk dQ reductions (one query tile of fp32).
+  static constexpr uint32_t STG_BYTES = DQ ? BM * D * 4 : 0;
   static constexpr uint32_t OFF_BAR = OFF_STG + STG_BYTES;
   static constexpr int B_KV = 0, B_QDFULL = 1, B_QDEMPTY = 1 + QS, B_SDP = 1 + 2 * QS,
                        B_PDS = B_SDP + 1, B_MMA = B_PDS + 1, B_DQFULL = B_MMA + 1,
@@ -810,14 +822,6 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(C::B_DQFREE));
           const int q0 = (I.qt0 + i) * BM;
-          if constexpr (C::DQ_T) {
-            // lanes = d index lr, columns = query q of the tile: for each q the warp
-            // adds 32 consecutive floats of accumulator row q (one 128-byte line).
-            float* rows = p.dqacc + ((size_t)I.bh * p.Npad + (size_t)q0) * D;
-#pragma unroll
-            for (int q = 0; q < COLS; ++q) red_add_f32(rows + q * D + dq_swz(q, lr), __uint_as_float(v[q]));
-            continue;
-          }
           // The previous bulk reduction must have finished reading the staging tile.
           if (leader) {
             bulk_wait_read0();
@@ -827,7 +831,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
             ok = false;
             break;
           }
-          {
+          if constexpr (C::DQ_T) {
+            // lanes = d index lr, columns = query q: 32 lanes write 128 contiguous bytes of row q
+#pragma unroll
+            for (int q = 0; q < COLS; ++q) stg[q * D + dq_swz(q, lr)] = __uint_as_float(v[q]);
+          } else {
             // lanes = query row lr, columns = d
 #pragma unroll
             for (int c = 0; c < COLS; c += 4)

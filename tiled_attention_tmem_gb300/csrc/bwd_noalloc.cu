@@ -116,7 +116,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
 
   if (five) {
     ConvParams cp{dqacc, static_cast<uint16_t*>(dq), N, Npad, BH, scale};
-    const long long groups = (long long)BH * N * D / 4;
+    const long long groups = (long long)BH * N * D / 8;  // 8 columns per thread
     bwd_conv_kernel<D><<<(unsigned)std::min<long long>((groups + 255) / 256, (long long)sms() * 8), 256, 0, st>>>(cp);
     if ((e = cudaGetLastError()) != cudaSuccess) return record_cuda_error(e);
     return FA_OK;
@@ -144,7 +144,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
 
 // Same tile configurations as the workspace-taking backward.
 using NKV5_64 = BwdKVCfg<64, 128, true, 1, 2, false>;
-using NKV5_128 = BwdKVCfg<128, 64, true, 1, 4, true>;
+using NKV5_128 = BwdKVCfg<128, 64, true, 1, 3, true>;
 using NKV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
 using NKV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
 using NKV7_256 = BwdKVCfg<256, 64, false, 2, 1, false>;

@@ -89,10 +89,6 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, uint32_t ssrc, 
       "r"(ssrc), "r"(bytes)
       : "memory");
 }
-// Element-wise fp32 reduction into global memory (performed at L2).
-__device__ __forceinline__ void red_add_f32(float* gaddr, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gaddr), "f"(v) : "memory");
-}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
