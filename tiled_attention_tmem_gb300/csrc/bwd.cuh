@@ -228,9 +228,9 @@ struct BwdKVCfg {
   static constexpr int THREADS = 128 * (1 + NCW + (DQ ? 1 : 0));
   // setmaxnreg budgets per warpgroup (producer/MMA, compute, dQ drain): the sum
   // over warpgroups stays within the launch's THREADS * (65536 / THREADS),
-  // i.e. 72 + 2 * 160 + 120 = 512 at 512 threads and 96 + 224 + 168 <= 3 * 168.
+  // i.e. 72 + 2 * 160 + 120 = 512 at 512 threads and 104 + 224 + 168 <= 3 * 168.
   static constexpr int REG_LAUNCH = 65536 / THREADS >= 256 ? 255 : (65536 / THREADS) / 8 * 8;
-  static constexpr int REG_LOW = THREADS == 512 ? 72 : 96;
+  static constexpr int REG_LOW = THREADS == 512 ? 72 : 104;
   static constexpr int REG_COMPUTE = THREADS == 512 ? 160 : (NCW == 2 ? 208 : 224);
   static constexpr int REG_DRAIN = THREADS == 512 ? 120 : REG_LAUNCH;
   static_assert(THREADS < 384 || REG_LOW + NCW * REG_COMPUTE + (DQ ? REG_DRAIN : 0) <= THREADS / 128 * REG_LAUNCH,
@@ -433,7 +433,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
       // blocked on a commit or a wait no longer leaves the tensor pipe idle.
       // Each issuing thread commits to KVEMPTY after its last MMA of an item
       // that reads K or V.
-      if (lane == 0) {
+      {
         constexpr uint32_t idS = make_idesc(128, BM, false, false);
         constexpr uint32_t idAcc = make_idesc(128, DH, false, true);
         const uint32_t kt = sbase + C::OFF_K, vt = sbase + C::OFF_V;
@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         auto issue_tail = [&](int g, int s, int h, bool first) -> bool {
           issue_acc(s, h, first);
           if constexpr (C::DQ) {
-            if (g > 0 && !wait_one(BAR(C::B_DQFREE), (g - 1) & 1, ab, (kKBwdKV << 8) | 6)) return false;
+            if (g > 0 && !wait_warp(BAR(C::B_DQFREE), (g - 1) & 1, ab, (kKBwdKV << 8) | 6)) return false;
             tc_fence_after();
             issue_dq();
           }
@@ -495,15 +495,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         if (C::EARLY && warp == 1) {
           // S^T(g), dP^T(g) as soon as the compute warps hold S^T(g-1), dP^T(g-1) in registers.
           for (int r = 0; ok; ++r) {
-            const int w = item_one(r);
+            const int w = item_warp(r);
             if (w < 0 || w >= p.items) break;
             const int n = coords(w).n;
             if (n <= 0) continue;
-            if (!wait_one(BAR(C::B_KV), nkv & 1, ab, (kKBwdKV << 8) | 2)) break;
+            if (!wait_warp(BAR(C::B_KV), nkv & 1, ab, (kKBwdKV << 8) | 2)) break;
             for (int i = 0; i < n; ++i, ++g) {
               const int s = g % QS;
-              if ((g > 0 && !wait_one(BAR(C::B_SCONS), (g - 1) & 1, ab, (kKBwdKV << 8) | 14)) ||
-                  !wait_one(BAR(C::B_QDFULL + s), (g / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
+              if ((g > 0 && !wait_warp(BAR(C::B_SCONS), (g - 1) & 1, ab, (kKBwdKV << 8) | 14)) ||
+                  !wait_warp(BAR(C::B_QDFULL + s), (g / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
                 ok = false;
                 break;
               }
@@ -516,13 +516,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           }
         } else if (C::EARLY) {
           for (int r = 0; ok; ++r) {
-            const int w = item_one(r);
+            const int w = item_warp(r);
             if (w < 0 || w >= p.items) break;
             const Item I = coords(w);
             if (I.n <= 0) continue;
             for (int i = 0; i < I.n; ++i, ++g) {
               const int s = g % QS;
-              if (!wait_one(BAR(C::B_PDS), g & 1, ab, (kKBwdKV << 8) | 4)) {
+              if (!wait_warp(BAR(C::B_PDS), g & 1, ab, (kKBwdKV << 8) | 4)) {
                 ok = false;
                 break;
               }
@@ -537,26 +537,26 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           }
         } else {
           for (int r = 0; ok; ++r) {
-            const int w = item_one(r);
+            const int w = item_warp(r);
             if (w < 0 || w >= p.items) break;
             const Item I = coords(w);
             if (I.n <= 0) continue;
-            if (!wait_one(BAR(C::B_KV), nkv & 1, ab, (kKBwdKV << 8) | 2) ||
-                !wait_one(BAR(C::B_QDFULL + g % QS), (g / QS) & 1, ab, (kKBwdKV << 8) | 3))
+            if (!wait_warp(BAR(C::B_KV), nkv & 1, ab, (kKBwdKV << 8) | 2) ||
+                !wait_warp(BAR(C::B_QDFULL + g % QS), (g / QS) & 1, ab, (kKBwdKV << 8) | 3))
               break;
             tc_fence_after();
             issue_sdp(g % QS);
             for (int i = 0; i < I.n; ++i, ++g) {
               const int s = g % QS;
               const int s1 = (g + 1) % QS;
-              if (!wait_one(BAR(C::B_PDS), g & 1, ab, (kKBwdKV << 8) | 4)) {
+              if (!wait_warp(BAR(C::B_PDS), g & 1, ab, (kKBwdKV << 8) | 4)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
               // SEP: S^T / dP^T of the next query tile go ahead of dV, dK, dQ.
               if (C::SEP && i + 1 < I.n) {
-                if (!wait_one(BAR(C::B_QDFULL + s1), ((g + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
+                if (!wait_warp(BAR(C::B_QDFULL + s1), ((g + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
                   ok = false;
                   break;
                 }
@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
                 break;
               }
               if (!C::SEP && i + 1 < I.n) {
-                if (!wait_one(BAR(C::B_QDFULL + s1), ((g + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
+                if (!wait_warp(BAR(C::B_QDFULL + s1), ((g + 1) / QS) & 1, ab, (kKBwdKV << 8) | 5)) {
                   ok = false;
                   break;
                 }
@@ -1000,20 +1000,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
       }
       __syncwarp();
     } else if (warp == 1) {
-      if (lane == 0) {
+      {
         constexpr uint32_t idS = make_idesc(128, BN, false, false);
         constexpr uint32_t idQ = make_idesc(128, D, false, true);
-        bool ok = wait_one(BAR(C::B_QFULL), 0, ab, (kKBwdQ << 8) | 2);
+        bool ok = wait_warp(BAR(C::B_QFULL), 0, ab, (kKBwdQ << 8) | 2);
         int it = 0;
         for (int j = 0; ok && j < n; ++j) {
           const int sk = it % S;
-          if (!wait_one(BAR(C::B_KVFULL + sk), (it / S) & 1, ab, (kKBwdQ << 8) | 3)) {
+          if (!wait_warp(BAR(C::B_KVFULL + sk), (it / S) & 1, ab, (kKBwdQ << 8) | 3)) {
             ok = false;
             break;
           }
           ++it;
           const int sv = it % S;
-          if (!wait_one(BAR(C::B_KVFULL + sv), (it / S) & 1, ab, (kKBwdQ << 8) | 3)) {
+          if (!wait_warp(BAR(C::B_KVFULL + sv), (it / S) & 1, ab, (kKBwdQ << 8) | 3)) {
             ok = false;
             break;
           }
@@ -1031,7 +1031,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
                    desc_kmajor(vb, C::KV_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
           mma_commit(BAR(C::B_SDP));
           mma_commit(BAR(C::B_KVEMPTY + sv));
-          if (!wait_one(BAR(C::B_DS), j & 1, ab, (kKBwdQ << 8) | 4)) {
+          if (!wait_warp(BAR(C::B_DS), j & 1, ab, (kKBwdQ << 8) | 4)) {
             ok = false;
             break;
           }

@@ -161,11 +161,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
 
   // Two softmax warpgroups (384 threads, 168 registers each at launch): the
   // producer/MMA warpgroup gives registers to the softmax warpgroups;
-  // 128 * 80 + 256 * 208 stays within the 384 * 168 the block was launched with.
+  // 128 * 88 + 256 * 208 equals the 384 * 168 the block was launched with.
   constexpr bool kSplitRegs = C::THREADS == 384;
   if (!*abort_flag) {
     if (warp < 4) {
-    if constexpr (kSplitRegs) regs_shrink<80>();
+    if constexpr (kSplitRegs) regs_shrink<88>();
     if (warp == 0) {
       // ------------------------------------------------------------ producer
       if (lane == 0) {
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
       __syncwarp();
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issue
-      if (lane == 0) {
+      {
         constexpr uint32_t idS = make_idesc(128, BN, false, false);
         constexpr uint32_t idO = make_idesc(128, D, false, true);
         auto issue_s = [&](int t, int s) {
@@ -234,12 +234,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           const int w = item_of(r);
           if (w >= p.items) break;
           const Item I = coords(w);
-          ok = wait_one(BAR(C::B_QFULL), nitems & 1, ab, (kKFwd << 8) | 2);
+          ok = wait_warp(BAR(C::B_QFULL), nitems & 1, ab, (kKFwd << 8) | 2);
           ++nitems;
           if (!ok) break;
           {
             const int s = it % S;
-            ok = wait_one(BAR(C::B_KVFULL + s), (it / S) & 1, ab, (kKFwd << 8) | 3);
+            ok = wait_warp(BAR(C::B_KVFULL + s), (it / S) & 1, ab, (kKFwd << 8) | 3);
             if (!ok) break;
             tc_fence_after();
             for (int t = 0; t < NQ; ++t)
@@ -250,7 +250,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           }
           for (int j = 0; ok && j < I.nmax; ++j) {
             const int sv = it % S;
-            ok = wait_one(BAR(C::B_KVFULL + sv), (it / S) & 1, ab, (kKFwd << 8) | 4);
+            ok = wait_warp(BAR(C::B_KVFULL + sv), (it / S) & 1, ab, (kKFwd << 8) | 4);
             ++it;
             if (!ok) break;
             tc_fence_after();
@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
             const uint32_t vb = sbase + C::OFF_KV + sv * C::KV_TILE;
             for (int t = 0; t < NQ && ok; ++t) {
               if (j < I.nkv[t]) {
-                if (!wait_one(BAR(C::B_PREADY + t), (g[t] + j) & 1, ab, (kKFwd << 8) | 5)) {
+                if (!wait_warp(BAR(C::B_PREADY + t), (g[t] + j) & 1, ab, (kKFwd << 8) | 5)) {
                   ok = false;
                   break;
                 }
@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
               }
               if (j + 1 < I.nkv[t]) {
                 if (!k_ready) {
-                  if (!wait_one(BAR(C::B_KVFULL + sk), (it / S) & 1, ab, (kKFwd << 8) | 6)) {
+                  if (!wait_warp(BAR(C::B_KVFULL + sk), (it / S) & 1, ab, (kKFwd << 8) | 6)) {
                     ok = false;
                     break;
                   }
