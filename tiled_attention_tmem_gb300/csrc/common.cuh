@@ -52,6 +52,21 @@ __device__ __forceinline__ bool wait_warp(uint32_t bar, uint32_t parity, const C
   return __all_sync(0xffffffffu, ok);
 }
 
+// Bounded wait until a shared-memory counter written by another warp of the
+// CTA reaches `target`.
+__device__ __forceinline__ bool wait_count(const volatile int* cnt, int target, const CtaAbort& ab, int where) {
+  if (*cnt >= target) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (*cnt >= target) return true;
+    if (*ab.flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      raise_timeout(ab, where);
+      return false;
+    }
+  }
+}
+
 // Launch order with L2 locality.  Blocks are grouped by heads: a group holds
 // `group` consecutive heads and all of their `tiles` tiles, so the blocks that
 // share a head's K/V (forward) or Q/dO (backward) run at the same time and read
