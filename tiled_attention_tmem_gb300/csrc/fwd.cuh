@@ -55,7 +55,9 @@ struct FwdCfg {
   static constexpr uint32_t KV_TILE = PANELS * KV_PANEL;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_KV = OFF_Q + NQ * Q_TILE;
-  static constexpr uint32_t OFF_BAR = OFF_KV + STAGES * KV_TILE;
+  // O epilogue staging: 2 KB per softmax warp (32 rows x 32 bf16 columns).
+  static constexpr uint32_t OFF_EPI = OFF_KV + STAGES * KV_TILE;
+  static constexpr uint32_t OFF_BAR = OFF_EPI + NQ * 4 * 2048;
   // barriers: q_full, kv_full[S], kv_empty[S], s_full[NQ], p_ready[NQ], o_ready[NQ], done
   static constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES,
                        B_SFULL = 1 + 2 * STAGES, B_PREADY = B_SFULL + NQ,
@@ -411,7 +413,12 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           tc_fence_after();
           const float inv = 1.f / l;
           const bool store = qi < p.N;
-          uint16_t* orow = p.o + ((size_t)bh * p.N + (size_t)(store ? qi : 0)) * D;
+          // Staged through this warp's 2 KB of shared memory, 32 columns at a
+          // time: each thread writes its row, then each warp store covers 8 rows
+          // x 64 contiguous bytes instead of 32 rows x 16 bytes.
+          uint8_t* epi = gbase + C::OFF_EPI + (t * 4 + quad) * 2048;
+          const int row0 = I.q0 + 128 * t + quad * 32;  // this warp's first query row
+          uint16_t* obase = p.o + ((size_t)bh * p.N + (size_t)row0) * D;
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t orr[32];
@@ -422,12 +429,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
 #pragma unroll
             for (int e = 0; e < 32; e += 2)
               pk[e >> 1] = pack_bf16(__uint_as_float(orr[e]) * inv, __uint_as_float(orr[e + 1]) * inv);
-            if (store) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
 #pragma unroll
-              for (int v = 0; v < 4; ++v)
-                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(epi + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const int rr = j * 8 + (lane >> 2), u = lane & 3;
+              const uint4 val = *reinterpret_cast<const uint4*>(epi + rr * 64 + ((u ^ ((rr >> 1) & 3)) << 4));
+              if (row0 + rr < p.N) *reinterpret_cast<uint4*>(obase + (size_t)rr * D + c0 + 8 * u) = val;
             }
+            __syncwarp();
           }
           if (store) p.lse[(size_t)bh * p.N + qi] = (m_used + log2f(l)) * kLn2;
         }
