@@ -54,11 +54,7 @@ fa_status run_pre(const void* o, const void* dO, const float* lse, const Workspa
               N, Npad, BH, D, w.sched};
   const long long threads = (long long)BH * Npad * (D / 8);
   const long long blocks = std::min<long long>((threads + 255) / 256, (long long)sm_count() * 8);
-  prof_before(FA_KERNEL_BWD_PRE, st);
-  bwd_pre_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
-  prof_after(FA_KERNEL_BWD_PRE, st);
-  return e == cudaSuccess ? FA_OK : record_cuda_error(e);
+  return launch(FA_KERNEL_BWD_PRE, bwd_pre_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, st, p);
 }
 
 template <int D>
@@ -66,11 +62,7 @@ fa_status run_conv(const Workspace& w, void* dq, int BH, int N, int Npad, float 
   ConvParams p{w.dqacc, static_cast<uint16_t*>(dq), N, Npad, BH, scale};
   const long long groups = (long long)BH * N * D / 8;  // 8 columns per thread
   const long long blocks = std::min<long long>((groups + 255) / 256, (long long)sm_count() * 8);
-  prof_before(FA_KERNEL_BWD_CONV, st);
-  bwd_conv_kernel<D><<<(unsigned)blocks, 256, 0, st>>>(p);
-  cudaError_t e = cudaGetLastError();
-  prof_after(FA_KERNEL_BWD_CONV, st);
-  return e == cudaSuccess ? FA_OK : record_cuda_error(e);
+  return launch(FA_KERNEL_BWD_CONV, bwd_conv_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, st, p);
 }
 
 template <class C>

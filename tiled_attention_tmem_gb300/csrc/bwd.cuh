@@ -61,6 +61,7 @@ struct PreParams {
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
+  grid_dep_wait();
   constexpr int G = D / 8;
   const long long rows = (long long)p.BH * p.Npad;
   const int sub = threadIdx.x % G;
@@ -105,6 +106,7 @@ struct ConvParams {
 
 template <int D>
 __global__ void __launch_bounds__(256) bwd_conv_kernel(const ConvParams p) {
+  grid_dep_wait();
   // Each thread converts 8 consecutive columns (two 16-byte loads, one 16-byte
   // store); two groups per iteration keep four loads in flight.
   const long long n8 = (long long)p.BH * p.N * D / 8;
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
   if (threadIdx.x == 0) {
-    *abort_flag = (*reinterpret_cast<volatile int*>(p.err) != 0) ? 1 : 0;
+    *abort_flag = 0;
     *tails_issued = 0;
     mbar_init(BAR(C::B_KV), 1);
     mbar_init(BAR(C::B_KVEMPTY), C::EARLY ? 2 : 1);
@@ -292,6 +294,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const CtaAbort ab{abort_flag, p.err};
+  grid_dep_wait();
+  // A kernel that gave up earlier left the error word set: do nothing.
+  const bool skip = *reinterpret_cast<volatile int*>(p.err) != 0;
 
   // Persistent work loop.  Work item w = (key tile, d part, head) in launch
   // order: heads in groups for L2 reuse of their Q, dO and dQ accumulator,
@@ -345,7 +350,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
   // register budget (REG_LOW, REG_COMPUTE, REG_DRAIN): the producer/MMA
   // warpgroup gives registers to the compute warpgroup(s).
   constexpr bool kSplitRegs = C::THREADS >= 384;
-  if (!*abort_flag) {
+  if (!skip) {
     if (warp < 4) {
     if constexpr (kSplitRegs) regs_shrink<C::REG_LOW>();
     if (warp == 0) {
@@ -938,7 +943,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
   if (threadIdx.x == 0) {
-    *abort_flag = (*reinterpret_cast<volatile int*>(p.err) != 0) ? 1 : 0;
+    *abort_flag = 0;
     mbar_init(BAR(C::B_QFULL), 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(BAR(C::B_KVFULL + s), 1);
@@ -959,6 +964,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const CtaAbort ab{abort_flag, p.err};
+  grid_dep_wait();
+  // A kernel that gave up earlier left the error word set: do nothing.
+  const bool skip = *reinterpret_cast<volatile int*>(p.err) != 0;
 
   const int n_qt = (p.N + 127) / 128;
   int qt, bh;
@@ -971,7 +979,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
     n = last / BN + 1;
   }
 
-  if (!*abort_flag) {
+  if (!skip) {
     if (warp == 0) {
       if (lane == 0) {
         tma_prefetch_desc(&p.q_map);

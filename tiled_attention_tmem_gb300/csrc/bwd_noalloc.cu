@@ -81,12 +81,13 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   PreParams pp{static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, lse2, dd, dqacc, N, Npad,
                BH, D, sched};
   const long long pre_threads = (long long)BH * Npad * (D / 8);
-  bwd_pre_kernel<D><<<(unsigned)std::min<long long>((pre_threads + 255) / 256, (long long)sms() * 8), 256, 0, st>>>(pp);
-  if ((e = cudaGetLastError()) != cudaSuccess) return record_cuda_error(e);
-
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
   fa_status s;
+  if ((s = launch(FA_KERNEL_BWD_PRE, bwd_pre_kernel<D>,
+                  dim3((unsigned)std::min<long long>((pre_threads + 255) / 256, (long long)sms() * 8)), dim3(256), 0,
+                  st, pp)) != FA_OK)
+    return s;
   BwdKVParams kp;
   if ((s = make_tile_map(&kp.q_map, q, bf, 2, D, N, BH, 64, KV::BM, sw)) != FA_OK) return s;
   if ((s = make_tile_map(&kp.do_map, dO, bf, 2, D, N, BH, 64, KV::BM, sw)) != FA_OK) return s;
@@ -117,9 +118,9 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   if (five) {
     ConvParams cp{dqacc, static_cast<uint16_t*>(dq), N, Npad, BH, scale};
     const long long groups = (long long)BH * N * D / 8;  // 8 columns per thread
-    bwd_conv_kernel<D><<<(unsigned)std::min<long long>((groups + 255) / 256, (long long)sms() * 8), 256, 0, st>>>(cp);
-    if ((e = cudaGetLastError()) != cudaSuccess) return record_cuda_error(e);
-    return FA_OK;
+    return launch(FA_KERNEL_BWD_CONV, bwd_conv_kernel<D>,
+                  dim3((unsigned)std::min<long long>((groups + 255) / 256, (long long)sms() * 8)), dim3(256), 0, st,
+                  cp);
   }
   BwdQParams qp;
   if ((s = make_tile_map(&qp.q_map, q, bf, 2, D, N, BH, 64, 128, sw)) != FA_OK) return s;

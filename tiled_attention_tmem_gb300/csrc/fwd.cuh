@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
   const int lane = lane_id();
 
   if (threadIdx.x == 0) {
-    *abort_flag = (*reinterpret_cast<volatile int*>(p.err) != 0) ? 1 : 0;
+    *abort_flag = 0;
     mbar_init(bar0 + 8 * C::B_QFULL, 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(bar0 + 8 * (C::B_KVFULL + s), 1);
@@ -130,6 +130,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
   const CtaAbort ab{abort_flag, p.err};
+  grid_dep_wait();
+  // A kernel that gave up earlier left the error word set: do nothing.
+  const bool skip = *reinterpret_cast<volatile int*>(p.err) != 0;
 
   // Persistent work loop.  Work item w is (query block, head) in launch order:
   // heads grouped for L2 reuse, and under the causal mask the query blocks with
@@ -165,7 +168,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
   // producer/MMA warpgroup gives registers to the softmax warpgroups;
   // 128 * 88 + 256 * 208 equals the 384 * 168 the block was launched with.
   constexpr bool kSplitRegs = C::THREADS == 384;
-  if (!*abort_flag) {
+  if (!skip) {
     if (warp < 4) {
     if constexpr (kSplitRegs) regs_shrink<88>();
     if (warp == 0) {

@@ -37,16 +37,31 @@ int sm_count_cached();
 void prof_before(int kind, cudaStream_t st);
 void prof_after(int kind, cudaStream_t st);
 
-// Kernel launch helper: sets the dynamic shared memory limit and launches.
+// Kernel launch helper: sets the dynamic shared memory limit and launches with
+// programmatic stream serialization, so the kernel can be scheduled while the
+// previous kernel in the stream finishes (every kernel of this library waits
+// for it with griddepcontrol.wait before touching memory).
 template <class Kernel, class Params>
 fa_status launch(int kind, Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t st,
                  const Params& p) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
-  if (e != cudaSuccess) return record_cuda_error(e);
+  cudaError_t e = cudaSuccess;
+  if (smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return record_cuda_error(e);
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_before(kind, st);
-  kernel<<<grid, block, smem, st>>>(p);
-  e = cudaGetLastError();
+  e = cudaLaunchKernelEx(&cfg, kernel, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   prof_after(kind, st);
   if (e != cudaSuccess) return record_cuda_error(e);
   return FA_OK;
