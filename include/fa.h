@@ -66,7 +66,8 @@ typedef enum {
 
 /*
  * Forward.  q, k, v: [B,H,N,d] bf16 (read).  o: [B,H,N,d] bf16 (written).
- * lse: [B,H,N] fp32 (written), natural log.  d must be 64, 128 or 256.
+ * lse: [B,H,N] fp32 (written), natural log.  d must be 64, 96, 128, 192 or 256
+ * (96 and 192 run the 128 / 256 kernels on zero-padded tiles).
  * scale: finite and > 0 (typically 1/sqrt(d)).  causal: 0 or 1 (key j is
  * visible to query i iff j <= i).  B*H*N == 0 is a no-op returning FA_OK.
  */
@@ -78,8 +79,10 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
  * (FA_BWD_AUTO: the largest over the variants).  0 for invalid shapes.
  *   log2-domain LSE per row:           4*B*H*Npad bytes
  *   D (fp32 row dot products dO.O):    4*B*H*Npad bytes
- *   5-GEMM only, fp32 dQ accumulator:  4*B*H*Npad*d bytes
- * with Npad = N rounded up to a multiple of 128, plus 256 bytes of alignment.
+ *   5-GEMM only, fp32 dQ accumulator:  4*B*H*Npad*Dk bytes (Dk = 64 or 128: the
+ *                                      kernel head dim, 128 for d = 96)
+ *   work-item counters:                256 bytes
+ * with Npad = N rounded up to a multiple of 128.  5-GEMM: d <= 128.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int variant);
 

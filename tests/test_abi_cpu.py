@@ -50,7 +50,8 @@ def test_fwd_validation(lib):
         a = {**ok, **kw}
         return b.fa_fwd(q, k, v, o, lse, a["B"], a["H"], a["N"], a["d"], a["scale"], a["causal"], None)
 
-    assert call(d=96) == b.FA_ERR_UNSUPPORTED
+    assert call(d=80) == b.FA_ERR_UNSUPPORTED
+    assert call(d=160) == b.FA_ERR_UNSUPPORTED
     assert call(d=32) == b.FA_ERR_UNSUPPORTED
     assert call(N=-1) == b.FA_ERR_INVALID_ARG
     assert call(scale=0.0) == b.FA_ERR_INVALID_ARG
@@ -93,7 +94,7 @@ def test_bwd_validation(lib):
 
 
 def test_workspace_sizes(lib):
-    for d in (64, 128, 256):
+    for d in (64, 96, 128, 192, 256):
         w7 = b.fa_bwd_workspace_size(2, 3, 300, d, b.FA_BWD_7GEMM)
         assert w7 >= 4 * 6 * 384
         wa = b.fa_bwd_workspace_size(2, 3, 300, d, b.FA_BWD_AUTO)
@@ -101,6 +102,13 @@ def test_workspace_sizes(lib):
         if b.lib().fa_bwd_launches(2, 3, 300, d, b.FA_BWD_5GEMM, 0) > 0:
             w5 = b.fa_bwd_workspace_size(2, 3, 300, d, b.FA_BWD_5GEMM)
             assert w5 >= 4 * 6 * 384 * (d + 1)
+    # head dims 96 and 192 run on zero-padded 128 / 256 tiles: the fp32 dQ
+    # accumulator has the padded width
+    assert (b.fa_bwd_workspace_size(2, 3, 300, 96, b.FA_BWD_5GEMM)
+            == b.fa_bwd_workspace_size(2, 3, 300, 128, b.FA_BWD_5GEMM))
+    assert b.fa_bwd_workspace_size(2, 3, 300, 192, b.FA_BWD_5GEMM) == 0 or \
+        b.lib().fa_bwd_launches(2, 3, 300, 192, b.FA_BWD_5GEMM, 0) == 0
+    assert b.fa_bwd_choose(1, 1, 128, 192, 0) == b.FA_BWD_7GEMM
     assert b.fa_bwd_workspace_size(1, 1, 128, 100, b.FA_BWD_AUTO) == 0
     assert b.fa_bwd_workspace_size(1, 1, 128, 64, 9) == 0
 

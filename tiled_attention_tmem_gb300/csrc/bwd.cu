@@ -49,33 +49,33 @@ int sm_count() {
 
 template <int D>
 fa_status run_pre(const void* o, const void* dO, const float* lse, const Workspace& w, int BH, int N, int Npad,
-                  cudaStream_t st) {
+                  int hd, cudaStream_t st) {
   PreParams p{static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, w.lse2, w.dd, w.dqacc,
-              N, Npad, BH, D, w.sched};
+              N, Npad, BH, hd, w.sched};
   const long long threads = (long long)BH * Npad * (D / 8);
   const long long blocks = std::min<long long>((threads + 255) / 256, (long long)sm_count() * 8);
   return launch(FA_KERNEL_BWD_PRE, bwd_pre_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, st, p);
 }
 
 template <int D>
-fa_status run_conv(const Workspace& w, void* dq, int BH, int N, int Npad, float scale, cudaStream_t st) {
-  ConvParams p{w.dqacc, static_cast<uint16_t*>(dq), N, Npad, BH, scale};
-  const long long groups = (long long)BH * N * D / 8;  // 8 columns per thread
+fa_status run_conv(const Workspace& w, void* dq, int BH, int N, int Npad, int hd, float scale, cudaStream_t st) {
+  ConvParams p{w.dqacc, static_cast<uint16_t*>(dq), N, Npad, BH, hd, scale};
+  const long long groups = (long long)BH * N * hd / 8;  // 8 columns per thread
   const long long blocks = std::min<long long>((groups + 255) / 256, (long long)sm_count() * 8);
   return launch(FA_KERNEL_BWD_CONV, bwd_conv_kernel<D>, dim3((unsigned)blocks), dim3(256), 0, st, p);
 }
 
 template <class C>
 fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, const Workspace& w, void* dk,
-                 void* dv, int BH, int N, int Npad, float scale, int causal, cudaStream_t st) {
+                 void* dv, int BH, int N, int Npad, int hd, float scale, int causal, cudaStream_t st) {
   BwdKVParams p;
   fa_status s;
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
-  if ((s = make_tile_map(&p.q_map, q, bf, 2, C::D, N, BH, 64, C::BM, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&p.do_map, dO, bf, 2, C::D, N, BH, 64, C::BM, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&p.k_map, k, bf, 2, C::D, N, BH, 64, C::BN, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&p.v_map, v, bf, 2, C::D, N, BH, 64, C::BN, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&p.q_map, q, bf, 2, hd, N, BH, 64, C::BM, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&p.do_map, dO, bf, 2, hd, N, BH, 64, C::BM, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&p.k_map, k, bf, 2, hd, N, BH, 64, C::BN, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&p.v_map, v, bf, 2, hd, N, BH, 64, C::BN, sw)) != FA_OK) return s;
   p.lse2 = w.lse2;
   p.dd = w.dd;
   p.dqacc = w.dqacc;
@@ -86,6 +86,7 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
   p.N = N;
   p.Npad = Npad;
   p.BH = BH;
+  p.hd = hd;
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
@@ -102,15 +103,15 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
 
 template <class C>
 fa_status run_q(const void* q, const void* k, const void* v, const void* dO, const Workspace& w, void* dq, int BH,
-                int N, int Npad, float scale, int causal, cudaStream_t st) {
+                int N, int Npad, int hd, float scale, int causal, cudaStream_t st) {
   BwdQParams p;
   fa_status s;
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
-  if ((s = make_tile_map(&p.q_map, q, bf, 2, C::D, N, BH, 64, 128, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&p.do_map, dO, bf, 2, C::D, N, BH, 64, 128, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&p.k_map, k, bf, 2, C::D, N, BH, 64, C::BN, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&p.v_map, v, bf, 2, C::D, N, BH, 64, C::BN, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&p.q_map, q, bf, 2, hd, N, BH, 64, 128, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&p.do_map, dO, bf, 2, hd, N, BH, 64, 128, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&p.k_map, k, bf, 2, hd, N, BH, 64, C::BN, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&p.v_map, v, bf, 2, hd, N, BH, 64, C::BN, sw)) != FA_OK) return s;
   p.lse2 = w.lse2;
   p.dd = w.dd;
   p.dq = static_cast<uint16_t*>(dq);
@@ -119,6 +120,7 @@ fa_status run_q(const void* q, const void* k, const void* v, const void* dO, con
   p.N = N;
   p.Npad = Npad;
   p.BH = BH;
+  p.hd = hd;
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
@@ -130,46 +132,49 @@ fa_status run_q(const void* q, const void* k, const void* v, const void* dO, con
 
 template <int D, class KV5, class KV7, class Q7>
 fa_status run_d(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-                void* dq, void* dk, void* dv, int BH, int N, float scale, int causal, int variant, void* ws,
+                void* dq, void* dk, void* dv, int BH, int N, int hd, float scale, int causal, int variant, void* ws,
                 cudaStream_t st) {
   const int Npad = (N + 127) / 128 * 128;
   const bool five = variant == FA_BWD_5GEMM;
   const Workspace w = carve(ws, BH, Npad, D, five);
-  fa_status s = run_pre<D>(o, dO, lse, w, BH, N, Npad, st);
+  fa_status s = run_pre<D>(o, dO, lse, w, BH, N, Npad, hd, st);
   if (s != FA_OK) return s;
   if (five) {
     if constexpr (!std::is_same<KV5, void>::value) {
-      if ((s = run_kv<KV5>(q, k, v, dO, w, dk, dv, BH, N, Npad, scale, causal, st)) != FA_OK) return s;
-      return run_conv<D>(w, dq, BH, N, Npad, scale, st);
+      if ((s = run_kv<KV5>(q, k, v, dO, w, dk, dv, BH, N, Npad, hd, scale, causal, st)) != FA_OK) return s;
+      return run_conv<D>(w, dq, BH, N, Npad, hd, scale, st);
     }
     return FA_ERR_UNSUPPORTED;
   }
-  if ((s = run_kv<KV7>(q, k, v, dO, w, dk, dv, BH, N, Npad, scale, causal, st)) != FA_OK) return s;
-  return run_q<Q7>(q, k, v, dO, w, dq, BH, N, Npad, scale, causal, st);
+  if ((s = run_kv<KV7>(q, k, v, dO, w, dk, dv, BH, N, Npad, hd, scale, causal, st)) != FA_OK) return s;
+  return run_q<Q7>(q, k, v, dO, w, dq, BH, N, Npad, hd, scale, causal, st);
 }
 
 }  // namespace
 
+// d = 96 and d = 192 run the d = 128 and d = 256 kernels on zero-padded tiles
+// (TMA reads the columns past d as zeros; nothing past d is stored).
 fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                   void* dq, void* dk, void* dv, int BH, int N, int d, float scale, int causal, int variant,
                   void* workspace, cudaStream_t st) {
-  switch (d) {
+  switch (padded_head_dim(d)) {
     case 64:
-      return run_d<64, KV5_64, KV7_64, Q7_64>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, scale, causal, variant,
+      return run_d<64, KV5_64, KV7_64, Q7_64>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, variant,
                                               workspace, st);
     case 128:
-      return run_d<128, KV5_128, KV7_128, Q7_128>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, scale, causal, variant,
-                                                  workspace, st);
+      return run_d<128, KV5_128, KV7_128, Q7_128>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal,
+                                                  variant, workspace, st);
     case 256:
-      return run_d<256, void, KV7_256, Q7_256>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, scale, causal, variant,
+      return run_d<256, void, KV7_256, Q7_256>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, variant,
                                                workspace, st);
   }
   return FA_ERR_UNSUPPORTED;
 }
 
 bool bwd_supported(int d, int variant) {
-  if (variant == FA_BWD_7GEMM) return d == 64 || d == 128 || d == 256;
-  if (variant == FA_BWD_5GEMM) return d == 64 || d == 128;
+  const int D = padded_head_dim(d);
+  if (variant == FA_BWD_7GEMM) return D != 0;
+  if (variant == FA_BWD_5GEMM) return D == 64 || D == 128;
   return false;
 }
 

@@ -55,7 +55,7 @@ struct PreParams {
   float* lse2;
   float* dd;
   float* dqacc;  // nullptr for the 7-GEMM variant
-  int N, Npad, BH, d;
+  int N, Npad, BH, dv;  // dv: head dim of O and dO (<= D; the kernel's D covers padded columns)
   int* sched;    // work-item counters of the following kernels, zeroed here
 };
 
@@ -70,8 +70,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
     const int bh = (int)(row / p.Npad);
     const int i = (int)(row % p.Npad);
     float acc = 0.f;
-    if (i < p.N) {
-      const size_t off = ((size_t)bh * p.N + i) * D + sub * 8;
+    if (i < p.N && sub * 8 < p.dv) {
+      const size_t off = ((size_t)bh * p.N + i) * p.dv + sub * 8;
       const uint4 a = *reinterpret_cast<const uint4*>(p.o + off);
       const uint4 b = *reinterpret_cast<const uint4*>(p.dO + off);
       const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
@@ -98,9 +98,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
 
 // --------------------------------------------------------------- dQ convert
 struct ConvParams {
-  const float* dqacc;
-  uint16_t* dq;
-  int N, Npad, BH;
+  const float* dqacc;  // [bh][Npad][D], D = padded head dim
+  uint16_t* dq;        // [bh][N][dv]
+  int N, Npad, BH, dv;
   float scale;
 };
 
@@ -109,12 +109,12 @@ __global__ void __launch_bounds__(256) bwd_conv_kernel(const ConvParams p) {
   grid_dep_wait();
   // Each thread converts 8 consecutive columns (two 16-byte loads, one 16-byte
   // store); two groups per iteration keep four loads in flight.
-  const long long n8 = (long long)p.BH * p.N * D / 8;
+  const long long n8 = (long long)p.BH * p.N * p.dv / 8;
   const long long stride = (long long)gridDim.x * 256;
   auto convert = [&](long long g) {
     const long long e = g * 8;
-    const int c = (int)(e % D);
-    const long long rowg = e / D;  // bh * N + i
+    const int c = (int)(e % p.dv);
+    const long long rowg = e / p.dv;  // bh * N + i
     const int bh = (int)(rowg / p.N);
     const int i = (int)(rowg % p.N);
     const float* row = p.dqacc + ((size_t)bh * p.Npad + i) * D;
@@ -166,6 +166,7 @@ struct BwdKVParams {
   uint16_t* dv;
   int* err;
   int N, Npad, BH;
+  int hd;  // head dim of the tensors (<= D; tile columns past it read as 0 and are not stored)
   float scale_log2;
   float scale;
   int causal;
@@ -620,8 +621,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           // No query can see this key tile: zero gradients.
           if (key_ok && cw == 0)
             for (int c = 0; c < DH; c += 8) {
-              *reinterpret_cast<uint4*>(p.dv + ((size_t)I.bh * p.N + kj) * D + I.h * DH + c) = make_uint4(0, 0, 0, 0);
-              *reinterpret_cast<uint4*>(p.dk + ((size_t)I.bh * p.N + kj) * D + I.h * DH + c) = make_uint4(0, 0, 0, 0);
+              if (I.h * DH + c < p.hd) {
+                *reinterpret_cast<uint4*>(p.dv + ((size_t)I.bh * p.N + kj) * p.hd + I.h * DH + c) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(p.dk + ((size_t)I.bh * p.N + kj) * p.hd + I.h * DH + c) = make_uint4(0, 0, 0, 0);
+              }
             }
           continue;
         }
@@ -740,7 +743,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           if (C::NCW == 2 && which != cw) continue;  // two warpgroups: one stores dV, the other dK
-          uint16_t* dst = (which == 0 ? p.dv : p.dk) + (size_t)I.bh * p.N * D + I.h * DH;
+          uint16_t* dst = (which == 0 ? p.dv : p.dk) + (size_t)I.bh * p.N * p.hd + I.h * DH;
+          const int cols = min(DH, p.hd - I.h * DH);  // stored columns of this d part
           const float mul = which == 0 ? 1.f : p.scale;
           const uint32_t tacc = trow + (which == 0 ? C::T_DV : C::T_DK);
           if constexpr (C::DQ) {
@@ -777,12 +781,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
                 const int rr = quad * 32 + j * (32 / R) + lane / R;
                 const int u = lane % R;
                 const uint4 val = *ds_chunk(rr, u);
-                if (I.k0 + rr < p.N) *reinterpret_cast<uint4*>(dst + (size_t)(I.k0 + rr) * D + c0 + 8 * u) = val;
+                if (I.k0 + rr < p.N && c0 + 8 * u < cols)
+                  *reinterpret_cast<uint4*>(dst + (size_t)(I.k0 + rr) * p.hd + c0 + 8 * u) = val;
               }
               __syncwarp();
             }
           } else {
-            uint16_t* drow = dst + (size_t)(key_ok ? kj : 0) * D;
+            uint16_t* drow = dst + (size_t)(key_ok ? kj : 0) * p.hd;
 #pragma unroll
             for (int c0 = 0; c0 < DH; c0 += 32) {
               uint32_t rv[32];
@@ -796,7 +801,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
               if (key_ok) {
                 uint4* o4 = reinterpret_cast<uint4*>(drow + c0);
 #pragma unroll
-                for (int v = 0; v < 4; ++v) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                for (int v = 0; v < 4; ++v)
+                  if (c0 + 8 * v < cols) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
               }
             }
           }
@@ -901,6 +907,7 @@ struct BwdQParams {
   uint16_t* dq;
   int* err;
   int N, Npad, BH;
+  int hd;  // head dim of the tensors (<= D)
   float scale_log2;
   float scale;
   int causal;
@@ -1113,7 +1120,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
       if (ok && wait_warp(BAR(C::B_DQ), (n - 1) & 1, ab, (kKBwdQ << 8) | 6)) {
         tc_fence_after();
         const bool store = qi < p.N;
-        uint16_t* dst = p.dq + ((size_t)bh * p.N + (size_t)(store ? qi : 0)) * D;
+        uint16_t* dst = p.dq + ((size_t)bh * p.N + (size_t)(store ? qi : 0)) * p.hd;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t rr[32];
@@ -1127,7 +1134,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
           if (store) {
             uint4* o4 = reinterpret_cast<uint4*>(dst + c0);
 #pragma unroll
-            for (int v = 0; v < 4; ++v) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            for (int v = 0; v < 4; ++v)
+              if (c0 + 8 * v < p.hd) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           }
         }
       }

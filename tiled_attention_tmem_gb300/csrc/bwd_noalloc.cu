@@ -66,7 +66,7 @@ int sms() {
 
 template <class KV, class Q7, int D>
 fa_status run(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
-              void* dq, void* dk, void* dv, int BH, int N, float scale, int causal, bool five,
+              void* dq, void* dk, void* dv, int BH, int N, int hd, float scale, int causal, bool five,
               unsigned char* base, cudaStream_t st) {
   const int Npad = (N + 127) / 128 * 128;
   int* err = reinterpret_cast<int*>(base);
@@ -79,7 +79,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   if (e != cudaSuccess) return record_cuda_error(e);
 
   PreParams pp{static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(dO), lse, lse2, dd, dqacc, N, Npad,
-               BH, D, sched};
+               BH, hd, sched};
   const long long pre_threads = (long long)BH * Npad * (D / 8);
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const auto sw = CU_TENSOR_MAP_SWIZZLE_128B;
@@ -89,10 +89,10 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
                   st, pp)) != FA_OK)
     return s;
   BwdKVParams kp;
-  if ((s = make_tile_map(&kp.q_map, q, bf, 2, D, N, BH, 64, KV::BM, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&kp.do_map, dO, bf, 2, D, N, BH, 64, KV::BM, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&kp.k_map, k, bf, 2, D, N, BH, 64, KV::BN, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&kp.v_map, v, bf, 2, D, N, BH, 64, KV::BN, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&kp.q_map, q, bf, 2, hd, N, BH, 64, KV::BM, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&kp.do_map, dO, bf, 2, hd, N, BH, 64, KV::BM, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&kp.k_map, k, bf, 2, hd, N, BH, 64, KV::BN, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&kp.v_map, v, bf, 2, hd, N, BH, 64, KV::BN, sw)) != FA_OK) return s;
   kp.lse2 = lse2;
   kp.dd = dd;
   kp.dqacc = dqacc;
@@ -102,6 +102,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   kp.N = N;
   kp.Npad = Npad;
   kp.BH = BH;
+  kp.hd = hd;
   kp.scale_log2 = scale * kLog2e;
   kp.scale = scale;
   kp.causal = causal;
@@ -116,17 +117,17 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
     return s;
 
   if (five) {
-    ConvParams cp{dqacc, static_cast<uint16_t*>(dq), N, Npad, BH, scale};
-    const long long groups = (long long)BH * N * D / 8;  // 8 columns per thread
+    ConvParams cp{dqacc, static_cast<uint16_t*>(dq), N, Npad, BH, hd, scale};
+    const long long groups = (long long)BH * N * hd / 8;  // 8 columns per thread
     return launch(FA_KERNEL_BWD_CONV, bwd_conv_kernel<D>,
                   dim3((unsigned)std::min<long long>((groups + 255) / 256, (long long)sms() * 8)), dim3(256), 0, st,
                   cp);
   }
   BwdQParams qp;
-  if ((s = make_tile_map(&qp.q_map, q, bf, 2, D, N, BH, 64, 128, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&qp.do_map, dO, bf, 2, D, N, BH, 64, 128, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&qp.k_map, k, bf, 2, D, N, BH, 64, Q7::BN, sw)) != FA_OK) return s;
-  if ((s = make_tile_map(&qp.v_map, v, bf, 2, D, N, BH, 64, Q7::BN, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&qp.q_map, q, bf, 2, hd, N, BH, 64, 128, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&qp.do_map, dO, bf, 2, hd, N, BH, 64, 128, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&qp.k_map, k, bf, 2, hd, N, BH, 64, Q7::BN, sw)) != FA_OK) return s;
+  if ((s = make_tile_map(&qp.v_map, v, bf, 2, hd, N, BH, 64, Q7::BN, sw)) != FA_OK) return s;
   qp.lse2 = lse2;
   qp.dd = dd;
   qp.dq = static_cast<uint16_t*>(dq);
@@ -134,6 +135,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   qp.N = N;
   qp.Npad = Npad;
   qp.BH = BH;
+  qp.hd = hd;
   qp.scale_log2 = scale * kLog2e;
   qp.scale = scale;
   qp.causal = causal;
@@ -164,7 +166,8 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f) || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
   if (variant != FA_BWD_AUTO && variant != FA_BWD_5GEMM && variant != FA_BWD_7GEMM) return FA_ERR_INVALID_ARG;
-  if (d != 64 && d != 128 && d != 256) return FA_ERR_UNSUPPORTED;
+  const int D = padded_head_dim(d);  // 96 and 192 run on zero-padded 128 / 256 tiles
+  if (D == 0) return FA_ERR_UNSUPPORTED;
   if ((long long)B * H > 0x7fffffffLL || (long long)N > 0x7fffffffLL / 2) return FA_ERR_INVALID_ARG;
   if ((long long)B * H * N == 0) return FA_OK;
   if (!q || !k || !v || !o || !dO || !lse || !dq || !dk || !dv) return FA_ERR_INVALID_ARG;
@@ -176,20 +179,22 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   // The variant fa_bwd would run; with AUTO, fall back to the 7-GEMM form when
   // only its smaller scratch fits.  Anything beyond the static array is refused.
   bool five = (variant == FA_BWD_AUTO ? fa_bwd_choose(B, H, N, d, causal) : variant) == FA_BWD_5GEMM;
-  if (five && d == 256) return FA_ERR_UNSUPPORTED;
-  if (five && scratch_need(BH, Npad, d, true) > kScratchBytes && variant == FA_BWD_AUTO) five = false;
-  if (scratch_need(BH, Npad, d, five) > kScratchBytes) return FA_ERR_WORKSPACE;
+  if (five && D == 256) return FA_ERR_UNSUPPORTED;
+  if (five && scratch_need(BH, Npad, D, true) > kScratchBytes && variant == FA_BWD_AUTO) five = false;
+  if (scratch_need(BH, Npad, D, five) > kScratchBytes) return FA_ERR_WORKSPACE;
   unsigned char* base = scratch_address();
   if (!base) return FA_ERR_LAUNCH;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  switch (d) {
+  switch (D) {
     case 64:
-      return five ? run<NKV5_64, NQ7_64, 64>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, scale, causal, true, base, st)
-                  : run<NKV7_64, NQ7_64, 64>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, scale, causal, false, base, st);
+      return five ? run<NKV5_64, NQ7_64, 64>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, true, base, st)
+                  : run<NKV7_64, NQ7_64, 64>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, false, base, st);
     case 128:
-      return five ? run<NKV5_128, NQ7_128, 128>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, scale, causal, true, base, st)
-                  : run<NKV7_128, NQ7_128, 128>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, scale, causal, false, base, st);
+      return five ? run<NKV5_128, NQ7_128, 128>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, true, base,
+                                                st)
+                  : run<NKV7_128, NQ7_128, 128>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, false, base,
+                                                st);
     default:
-      return run<NKV7_256, NQ7_256, 256>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, scale, causal, false, base, st);
+      return run<NKV7_256, NQ7_256, 256>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, false, base, st);
   }
 }

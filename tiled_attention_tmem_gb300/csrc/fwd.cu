@@ -11,25 +11,29 @@ namespace {
 //  d = 64 : 2 x 128 query rows, 128 keys, 6 stages (Q 32 KiB + ring 96 KiB)
 //  d = 128: 2 x 128 query rows, 128 keys, 4 stages (Q 64 KiB + ring 128 KiB)
 //  d = 256: 1 x 128 query rows, 128 keys, 2 stages (Q 64 KiB + ring 128 KiB)
+// d = 96 and d = 192 run the d = 128 and d = 256 kernels: the TMA boxes read
+// columns past d as zeros, which leave S = QK^T unchanged and give zero
+// output columns that are not stored.
 using Fwd64 = FwdCfg<64, 2, 128, 6>;
 using Fwd128 = FwdCfg<128, 2, 128, 4>;
 using Fwd256 = FwdCfg<256, 1, 128, 2>;
 
 template <class C>
-fa_status run(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
+fa_status run(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N, int d,
               float scale, int causal, cudaStream_t st) {
   FwdParams p;
   fa_status s;
-  if ((s = make_tile_map(&p.q_map, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C::D, N, BH, 64, 128,
+  if ((s = make_tile_map(&p.q_map, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64, 128,
                          CU_TENSOR_MAP_SWIZZLE_128B)) != FA_OK)
     return s;
-  if ((s = make_tile_map(&p.k_map, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C::D, N, BH, 64, C::BN,
+  if ((s = make_tile_map(&p.k_map, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64, C::BN,
                          CU_TENSOR_MAP_SWIZZLE_128B)) != FA_OK)
     return s;
-  if ((s = make_tile_map(&p.v_map, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, C::D, N, BH, 64, C::BN,
+  if ((s = make_tile_map(&p.v_map, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64, C::BN,
                          CU_TENSOR_MAP_SWIZZLE_128B)) != FA_OK)
     return s;
   p.o = static_cast<uint16_t*>(o);
+  p.dv = d;
   p.lse = lse;
   p.err = device_error_word();
   if (!p.err) return record_cuda_error(cudaErrorMemoryAllocation);
@@ -53,9 +57,11 @@ fa_status run(const void* q, const void* k, const void* v, void* o, float* lse, 
 fa_status run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
                   int d, float scale, int causal, cudaStream_t st) {
   switch (d) {
-    case 64: return run<Fwd64>(q, k, v, o, lse, BH, N, scale, causal, st);
-    case 128: return run<Fwd128>(q, k, v, o, lse, BH, N, scale, causal, st);
-    case 256: return run<Fwd256>(q, k, v, o, lse, BH, N, scale, causal, st);
+    case 64: return run<Fwd64>(q, k, v, o, lse, BH, N, d, scale, causal, st);
+    case 96:
+    case 128: return run<Fwd128>(q, k, v, o, lse, BH, N, d, scale, causal, st);
+    case 192:
+    case 256: return run<Fwd256>(q, k, v, o, lse, BH, N, d, scale, causal, st);
   }
   return FA_ERR_UNSUPPORTED;
 }

@@ -33,6 +33,7 @@ struct FwdParams {
   CUtensorMap k_map;  // same tensor shape, box {64, BN, 1}
   CUtensorMap v_map;
   uint16_t* o;  // bf16 [B*H, N, d]
+  int dv;       // head dim d of the tensors (<= the kernel's D; columns d..D-1 of the tiles read as 0)
   float* lse;   // fp32 [B*H, N]
   int* err;
   int N;
@@ -421,7 +422,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           // x 64 contiguous bytes instead of 32 rows x 16 bytes.
           uint8_t* epi = gbase + C::OFF_EPI + (t * 4 + quad) * 2048;
           const int row0 = I.q0 + 128 * t + quad * 32;  // this warp's first query row
-          uint16_t* obase = p.o + ((size_t)bh * p.N + (size_t)row0) * D;
+          uint16_t* obase = p.o + ((size_t)bh * p.N + (size_t)row0) * p.dv;
 #pragma unroll
           for (int c0 = 0; c0 < D; c0 += 32) {
             uint32_t orr[32];
@@ -441,7 +442,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
             for (int j = 0; j < 4; ++j) {
               const int rr = j * 8 + (lane >> 2), u = lane & 3;
               const uint4 val = *reinterpret_cast<const uint4*>(epi + rr * 64 + ((u ^ ((rr >> 1) & 3)) << 4));
-              if (row0 + rr < p.N) *reinterpret_cast<uint4*>(obase + (size_t)rr * D + c0 + 8 * u) = val;
+              if (row0 + rr < p.N && c0 + 8 * u < p.dv)
+                *reinterpret_cast<uint4*>(obase + (size_t)rr * p.dv + c0 + 8 * u) = val;
             }
             __syncwarp();
           }

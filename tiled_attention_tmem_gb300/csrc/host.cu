@@ -34,7 +34,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-bool supported_d(int d) { return d == 64 || d == 128 || d == 256; }
+bool supported_d(int d) { return padded_head_dim(d) != 0; }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -181,7 +181,8 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, int variant) {
   const size_t bh = (size_t)B * H;
   const size_t npad = round_up((size_t)N, 128);
   size_t bytes = 2 * round_up(4 * bh * npad, 256);  // log2-domain LSE and D per padded row
-  if (variant != FA_BWD_7GEMM && bwd_supported(d, FA_BWD_5GEMM)) bytes += 4 * bh * npad * d;
+  if (variant != FA_BWD_7GEMM && bwd_supported(d, FA_BWD_5GEMM))
+    bytes += 4 * bh * npad * (size_t)padded_head_dim(d);  // fp32 dQ accumulator (padded head dim)
   return bytes + 256;
 }
 

@@ -72,6 +72,12 @@ fa_status run_fwd(const void* q, const void* k, const void* v, void* o, float* l
                   int d, float scale, int causal, cudaStream_t st);
 int fwd_launch_count(int d);
 
+// Head dims the kernels support and the kernel head dim (64, 128 or 256) that
+// serves each: 96 and 192 run on zero-padded 128 / 256 tiles.  0 if unsupported.
+inline int padded_head_dim(int d) {
+  return d == 64 ? 64 : (d == 96 || d == 128) ? 128 : (d == 192 || d == 256) ? 256 : 0;
+}
+
 // Backward launchers (bwd.cu).  Arguments already validated; workspace sized.
 fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO,
                   const float* lse, void* dq, void* dk, void* dv, int BH, int N, int d,
