@@ -97,7 +97,19 @@ def sweep_workloads() -> list[Workload]:
     return out
 
 
-WORKLOADS = {w.name: w for w in [TINY, CAUSAL_2K, KSHIFT_8K, HDIM256_4K] + sweep_workloads()}
+def head_dim_workloads() -> list[Workload]:
+    """Head-dim sweep: B=4, H=16, N=4096, d in {64, 96, 128, 192, 256}, both masks (10 points)."""
+    out = []
+    k = 0
+    for d in (64, 96, 128, 192, 256):
+        for causal in (False, True):
+            out.append(Workload(f"hdim_n4096_d{d}{'_causal' if causal else ''}", 4, 16, 4096, d, causal,
+                                seed=200 + k))
+            k += 1
+    return out
+
+
+WORKLOADS = {w.name: w for w in [TINY, CAUSAL_2K, KSHIFT_8K, HDIM256_4K] + sweep_workloads() + head_dim_workloads()}
 
 
 @dataclass
