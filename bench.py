@@ -315,6 +315,20 @@ def run_ours(args, rank, world, local_rank):
                  if n_ in kernels)
     bwd_tf = w.bwd_flops / (bwd_ms / 1e3) / 1e12 if bwd_ms else None
 
+    # The exp-unit bound of the method (one ex2 per score in the forward and the
+    # 5-GEMM backward, two in the 7-GEMM backward): nominal FLOPs per exp x the
+    # ex2 rate, measured at about 30 per clock per SM on this GPU (microbenchmark).
+    ex2_per_sm_clk = 30.0
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    clk = ((clocks or {}).get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))) * 1e6
+    ex2_rate = ex2_per_sm_clk * sms * clk
+    exps_bwd = 1 if chosen == b.FA_BWD_5GEMM else 2
+    exp_fwd_tf = 4 * w.d * ex2_rate / 1e12
+    exp_bwd_tf = 10 * w.d * ex2_rate / exps_bwd / 1e12
+    exp_bound = {"ex2_per_sm_clk": ex2_per_sm_clk, "fwd_tflops": exp_fwd_tf, "bwd_tflops": exp_bwd_tf,
+                 "fwd_frac": fwd_tf / exp_fwd_tf if fwd_tf else None,
+                 "bwd_frac": bwd_tf / exp_bwd_tf if bwd_tf else None}
+
     # End to end through the public API: pinned host inputs in, gradients and
     # forward outputs back to pinned host memory, every step.
     out_host = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (o, lse, *grads)]
@@ -361,7 +375,7 @@ def run_ours(args, rank, world, local_rank):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
             "frac_of_peak": frac, "peak_tflops": float(peaks["bf16_tflops"]),
-            "roofline": roof, "cpu_baseline": cpu,
+            "roofline": roof, "exp_bound": exp_bound, "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps},
             "gpu_launches": launches, "kernels": kernels,
