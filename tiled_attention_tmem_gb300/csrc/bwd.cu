@@ -90,7 +90,8 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
-  p.group = causal ? l2_head_group(N, C::D, BH) : head_group(((N + C::BN - 1) / C::BN) * C::DSPLIT, BH);
+  p.group = causal ? l2_head_group(N, C::D, BH, ((N + C::BN - 1) / C::BN) * C::DSPLIT)
+                   : head_group(((N + C::BN - 1) / C::BN) * C::DSPLIT, BH);
   p.sched = w.sched;
   const long long items = (long long)((N + C::BN - 1) / C::BN) * BH * C::DSPLIT;
   if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
@@ -124,10 +125,14 @@ fa_status run_q(const void* q, const void* k, const void* v, const void* dO, con
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
-  p.group = causal ? BH : head_group((N + 127) / 128, BH);
-  const long long blocks = (long long)((N + 127) / 128) * BH;
-  if (blocks > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
-  return launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<C>, dim3((unsigned)blocks), dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  p.group = causal ? l2_head_group(N, C::D, BH, (N + 127) / 128) : head_group((N + 127) / 128, BH);
+  p.sched = w.sched;
+  const long long items = (long long)((N + 127) / 128) * BH;
+  if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  p.items = (int)items;
+  // Persistent grid: one CTA per SM, each claiming work items.
+  const long long grid = std::min<long long>(items, sm_count_cached());
+  return launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<C>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, st, p);
 }
 
 template <int D, class KV5, class KV7, class Q7>

@@ -911,7 +911,9 @@ struct BwdQParams {
   float scale_log2;
   float scale;
   int causal;
-  int group;  // heads per launch-order group
+  int group;   // heads per launch-order group
+  int items;   // work items (query tiles x heads); the grid is persistent over them
+  int* sched;  // [1]: next unclaimed work item (zero at launch)
 };
 
 template <int D_, int BN_, int STAGES_>
@@ -923,11 +925,17 @@ struct BwdQCfg {
   static constexpr uint32_t KV_PANEL = BN * 128;
   static constexpr uint32_t KV_TILE = PANELS * KV_PANEL;
   static constexpr uint32_t OFF_Q = 0, OFF_DO = Q_TILE, OFF_KV = 2 * Q_TILE;
-  static constexpr uint32_t OFF_BAR = OFF_KV + STAGES * KV_TILE;
-  static constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES, B_SDP = 1 + 2 * STAGES,
-                       B_DS = B_SDP + 1, B_DQ = B_DS + 1, B_DONE = B_DQ + 1, NBAR = B_DONE + 1;
+  static constexpr uint32_t OFF_EPI = OFF_KV + STAGES * KV_TILE;
+  // dQ epilogue staging (2 KB per compute warp) where shared memory allows.
+  static constexpr uint32_t EPI_BYTES = OFF_EPI + 4 * 2048 + 512 + 1024 <= 232448 ? 4 * 2048 : 0;
+  static constexpr uint32_t OFF_BAR = OFF_EPI + EPI_BYTES;
+  static constexpr int IQ = 4;  // claimed work items passed from the producer to the other roles
+  static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 2 + STAGES, B_SDP = 2 + 2 * STAGES,
+                       B_DS = B_SDP + 1, B_DQ = B_DS + 1, B_DONE = B_DQ + 1, B_ITEMFULL = B_DONE + 1,
+                       B_ITEMEMPTY = B_ITEMFULL + IQ, NBAR = B_ITEMEMPTY + IQ;
+  static constexpr int ITEM_READERS = 1 + 4;  // the MMA warp and the four compute warps
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
-  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;
+  static constexpr uint32_t SMEM_BYTES = OFF_MISC + 32 + 1024;
   static constexpr int T_S = 0, T_DP = BN, T_DQ = 2 * BN;
   static constexpr int TMEM_USED = 2 * BN + D;
   static constexpr uint32_t TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
@@ -945,6 +953,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
   const uint32_t bar0 = sbase + C::OFF_BAR;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(gbase + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 4);
+  volatile int* item_ring = reinterpret_cast<volatile int*>(gbase + C::OFF_MISC + 16);
   const int warp = warp_id();
   const int lane = lane_id();
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
@@ -952,6 +961,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     mbar_init(BAR(C::B_QFULL), 1);
+    mbar_init(BAR(C::B_QEMPTY), 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(BAR(C::B_KVFULL + s), 1);
       mbar_init(BAR(C::B_KVEMPTY + s), 1);
@@ -960,6 +970,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
     mbar_init(BAR(C::B_DS), 4);
     mbar_init(BAR(C::B_DQ), 1);
     mbar_init(BAR(C::B_DONE), 1);
+    for (int k = 0; k < C::IQ; ++k) {
+      mbar_init(BAR(C::B_ITEMFULL + k), 1);
+      mbar_init(BAR(C::B_ITEMEMPTY + k), C::ITEM_READERS);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -975,16 +989,34 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
   // A kernel that gave up earlier left the error word set: do nothing.
   const bool skip = *reinterpret_cast<volatile int*>(p.err) != 0;
 
+  // Persistent work loop.  Work item w = (query tile of 128 rows, head) in
+  // launch order: heads grouped for L2 reuse of their K and V, and under the
+  // causal mask the query tiles that see the most key tiles first.  The
+  // producer claims items from a global counter one item ahead and passes them
+  // to the other roles through a shared-memory ring; barrier phases run on
+  // across items.
   const int n_qt = (p.N + 127) / 128;
-  int qt, bh;
-  grouped_order(blockIdx.x, n_qt, p.BH, p.group, qt, bh);
-  if (p.causal) qt = n_qt - 1 - qt;
-  const int q0 = qt * 128;
-  int n;
-  {
-    const int last = p.causal ? min(q0 + 127, p.N - 1) : p.N - 1;
-    n = last / BN + 1;
-  }
+  struct Item {
+    int q0, bh, n;  // first query row, head, key tiles
+  };
+  auto coords = [&](int w) {
+    Item I;
+    int qt;
+    grouped_order(w, n_qt, p.BH, p.group, qt, I.bh);
+    if (p.causal) qt = n_qt - 1 - qt;
+    I.q0 = qt * 128;
+    const int last = p.causal ? min(I.q0 + 127, p.N - 1) : p.N - 1;
+    I.n = last / BN + 1;
+    return I;
+  };
+  auto item_warp = [&](int t) -> int {
+    const int k = t % C::IQ;
+    if (!wait_warp(BAR(C::B_ITEMFULL + k), (t / C::IQ) & 1, ab, (kKBwdQ << 8) | 8)) return -1;
+    const int w = item_ring[k];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(BAR(C::B_ITEMEMPTY + k));
+    return w;
+  };
 
   if (!skip) {
     if (warp == 0) {
@@ -993,41 +1025,66 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
         tma_prefetch_desc(&p.do_map);
         tma_prefetch_desc(&p.k_map);
         tma_prefetch_desc(&p.v_map);
-        mbar_expect_tx(BAR(C::B_QFULL), 2 * C::Q_TILE);
-        for (int pn = 0; pn < C::PANELS; ++pn) {
-          tma_load_3d(sbase + C::OFF_Q + pn * C::Q_PANEL, &p.q_map, BAR(C::B_QFULL), 64 * pn, q0, bh);
-          tma_load_3d(sbase + C::OFF_DO + pn * C::Q_PANEL, &p.do_map, BAR(C::B_QFULL), 64 * pn, q0, bh);
-        }
-        int it = 0;
+        int it = 0, nitems = 0, published = 0;
         bool ok = true;
-        for (int j = 0; j < n && ok; ++j) {
-          for (int w = 0; w < 2; ++w) {
-            const int s = it % S;
-            if (!wait_one(BAR(C::B_KVEMPTY + s), ((it / S) & 1) ^ 1, ab, (kKBwdQ << 8) | 1)) {
-              ok = false;
-              break;
+        auto publish = [&](int w) -> bool {
+          const int k = published % C::IQ;
+          if (!wait_one(BAR(C::B_ITEMEMPTY + k), ((published / C::IQ) & 1) ^ 1, ab, (kKBwdQ << 8) | 9))
+            return false;
+          item_ring[k] = w;
+          mbar_arrive(BAR(C::B_ITEMFULL + k));
+          ++published;
+          return true;
+        };
+        int wn = atomicAdd(p.sched + 1, 1);
+        ok = publish(wn);
+        while (ok && wn < p.items) {
+          const Item I = coords(wn);
+          wn = atomicAdd(p.sched + 1, 1);
+          if (!publish(wn)) break;
+          // The previous item's last S / dP MMAs must be done reading Q and dO.
+          if (nitems > 0 && !wait_one(BAR(C::B_QEMPTY), (nitems - 1) & 1, ab, (kKBwdQ << 8) | 10)) break;
+          mbar_expect_tx(BAR(C::B_QFULL), 2 * C::Q_TILE);
+          for (int pn = 0; pn < C::PANELS; ++pn) {
+            tma_load_3d(sbase + C::OFF_Q + pn * C::Q_PANEL, &p.q_map, BAR(C::B_QFULL), 64 * pn, I.q0, I.bh);
+            tma_load_3d(sbase + C::OFF_DO + pn * C::Q_PANEL, &p.do_map, BAR(C::B_QFULL), 64 * pn, I.q0, I.bh);
+          }
+          ++nitems;
+          for (int j = 0; j < I.n && ok; ++j) {
+            for (int wkv = 0; wkv < 2; ++wkv) {
+              const int s = it % S;
+              if (!wait_one(BAR(C::B_KVEMPTY + s), ((it / S) & 1) ^ 1, ab, (kKBwdQ << 8) | 1)) {
+                ok = false;
+                break;
+              }
+              mbar_expect_tx(BAR(C::B_KVFULL + s), C::KV_TILE);
+              const CUtensorMap* m = wkv ? &p.v_map : &p.k_map;
+              for (int pn = 0; pn < C::PANELS; ++pn)
+                tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m, BAR(C::B_KVFULL + s),
+                            64 * pn, j * BN, I.bh);
+              if (j + 4 < I.n)
+                for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(m, 64 * pn, (j + 4) * BN, I.bh);
+              ++it;
             }
-            mbar_expect_tx(BAR(C::B_KVFULL + s), C::KV_TILE);
-            const CUtensorMap* m = w ? &p.v_map : &p.k_map;
-            for (int pn = 0; pn < C::PANELS; ++pn)
-              tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m, BAR(C::B_KVFULL + s), 64 * pn,
-                          j * BN, bh);
-            if (j + 4 < n)
-              for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(m, 64 * pn, (j + 4) * BN, bh);
-            ++it;
           }
         }
-        wait_drain_bwd(BAR(C::B_QFULL), 0);
+        if (nitems > 0) wait_drain_bwd(BAR(C::B_QFULL), (nitems - 1) & 1);
         for (int i = max(0, it - S); i < it; ++i) wait_drain_bwd(BAR(C::B_KVFULL + i % S), (i / S) & 1);
       }
       __syncwarp();
     } else if (warp == 1) {
-      {
-        constexpr uint32_t idS = make_idesc(128, BN, false, false);
-        constexpr uint32_t idQ = make_idesc(128, D, false, true);
-        bool ok = wait_warp(BAR(C::B_QFULL), 0, ab, (kKBwdQ << 8) | 2);
-        int it = 0;
-        for (int j = 0; ok && j < n; ++j) {
+      // Whole warp; one elected lane issues (see mma_ss).
+      constexpr uint32_t idS = make_idesc(128, BN, false, false);
+      constexpr uint32_t idQ = make_idesc(128, D, false, true);
+      bool ok = true;
+      int it = 0, gj = 0, nitems = 0;
+      for (int r = 0; ok; ++r) {
+        const int w = item_warp(r);
+        if (w < 0 || w >= p.items) break;
+        const Item I = coords(w);
+        if (!wait_warp(BAR(C::B_QFULL), nitems & 1, ab, (kKBwdQ << 8) | 2)) break;
+        ++nitems;
+        for (int j = 0; ok && j < I.n; ++j, ++gj) {
           const int sk = it % S;
           if (!wait_warp(BAR(C::B_KVFULL + sk), (it / S) & 1, ab, (kKBwdQ << 8) | 3)) {
             ok = false;
@@ -1053,7 +1110,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
                    desc_kmajor(vb, C::KV_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
           mma_commit(BAR(C::B_SDP));
           mma_commit(BAR(C::B_KVEMPTY + sv));
-          if (!wait_warp(BAR(C::B_DS), j & 1, ab, (kKBwdQ << 8) | 4)) {
+          if (j + 1 == I.n) mma_commit(BAR(C::B_QEMPTY));  // Q and dO no longer read
+          if (!wait_warp(BAR(C::B_DS), gj & 1, ab, (kKBwdQ << 8) | 4)) {
             ok = false;
             break;
           }
@@ -1065,79 +1123,107 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
           mma_commit(BAR(C::B_DQ));
           mma_commit(BAR(C::B_KVEMPTY + sk));
         }
-        mma_commit(BAR(C::B_DONE));
-        wait_drain_bwd(BAR(C::B_DONE), 0);
       }
+      mma_commit(BAR(C::B_DONE));
+      wait_drain_bwd(BAR(C::B_DONE), 0);
       __syncwarp();
     } else if (warp >= 4) {
       const int quad = warp & 3;
       const int r = quad * 32 + lane;
-      const int qi = q0 + r;
       const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
       const float cs = p.scale_log2;
-      const float l2 = p.lse2[(size_t)bh * p.Npad + qi];  // -inf past N: every p is 0
-      const float dd = p.dd[(size_t)bh * p.Npad + qi];
-      const float2 c2 = make_float2(cs, cs), l22 = make_float2(l2, l2), dd2 = make_float2(dd, dd);
-      const int limit = p.causal ? min(qi, p.N - 1) : p.N - 1;
+      const float2 c2 = make_float2(cs, cs);
       bool ok = true;
-      for (int j = 0; j < n; ++j) {
-        if (!wait_warp(BAR(C::B_SDP), j & 1, ab, (kKBwdQ << 8) | 5)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const int kbase = j * BN;
-#pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          uint32_t sr[32], dr[32];
-          tmem_ld_32x32b_x32(trow + C::T_S + c0, sr);
-          tmem_ld_32x32b_x32(trow + C::T_DP + c0, dr);
-          tmem_wait_ld();
-          reg_fence<32>(sr);
-          reg_fence<32>(dr);
-          uint32_t pk[16];
-          const bool masked = kbase + c0 + 31 > limit;
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float2 x = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, l22);
-            float2 pe = make_float2(ex2(x.x), ex2(x.y));
-            if (masked) {
-              if (kbase + c0 + e > limit) pe.x = 0.f;
-              if (kbase + c0 + e + 1 > limit) pe.y = 0.f;
-            }
-            const float2 ds =
-                fmul2(pe, fadd2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), dd2));
-            pk[e >> 1] = pack_bf16(ds.x, ds.y);
+      int gj = 0;
+      for (int rr = 0; ok; ++rr) {
+        const int w = item_warp(rr);
+        if (w < 0 || w >= p.items) break;
+        const Item I = coords(w);
+        const int qi = I.q0 + r;
+        const float l2 = p.lse2[(size_t)I.bh * p.Npad + qi];  // -inf past N: every p is 0
+        const float dd = p.dd[(size_t)I.bh * p.Npad + qi];
+        const float2 l22 = make_float2(l2, l2), dd2 = make_float2(dd, dd);
+        const int limit = p.causal ? min(qi, p.N - 1) : p.N - 1;
+        for (int j = 0; j < I.n; ++j, ++gj) {
+          if (!wait_warp(BAR(C::B_SDP), gj & 1, ab, (kKBwdQ << 8) | 5)) {
+            ok = false;
+            break;
           }
-          // dS (bf16) over the first half of dP's columns: chunk c0 -> columns c0/2.
-          tmem_st_32x32b_x16(trow + C::T_DP + (c0 >> 1), pk);
+          tc_fence_after();
+          const int kbase = j * BN;
+#pragma unroll
+          for (int c0 = 0; c0 < BN; c0 += 32) {
+            uint32_t sr[32], dr[32];
+            tmem_ld_32x32b_x32(trow + C::T_S + c0, sr);
+            tmem_ld_32x32b_x32(trow + C::T_DP + c0, dr);
+            tmem_wait_ld();
+            reg_fence<32>(sr);
+            reg_fence<32>(dr);
+            uint32_t pk[16];
+            const bool masked = kbase + c0 + 31 > limit;
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              const float2 x = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, l22);
+              float2 pe = make_float2(ex2(x.x), ex2(x.y));
+              if (masked) {
+                if (kbase + c0 + e > limit) pe.x = 0.f;
+                if (kbase + c0 + e + 1 > limit) pe.y = 0.f;
+              }
+              const float2 ds =
+                  fmul2(pe, fadd2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), dd2));
+              pk[e >> 1] = pack_bf16(ds.x, ds.y);
+            }
+            // dS (bf16) over the first half of dP's columns: chunk c0 -> columns c0/2.
+            tmem_st_32x32b_x16(trow + C::T_DP + (c0 >> 1), pk);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(C::B_DS));
         }
-        tmem_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(BAR(C::B_DS));
-      }
-      if (ok && wait_warp(BAR(C::B_DQ), (n - 1) & 1, ab, (kKBwdQ << 8) | 6)) {
+        if (!ok) break;
+        // dQ epilogue; its TMEM reads finish before these warps arrive on DS for
+        // the next item's first key tile, whose dQ MMA overwrites the accumulator.
+        if (!wait_warp(BAR(C::B_DQ), (gj - 1) & 1, ab, (kKBwdQ << 8) | 6)) break;
         tc_fence_after();
-        const bool store = qi < p.N;
-        uint16_t* dst = p.dq + ((size_t)bh * p.N + (size_t)(store ? qi : 0)) * p.hd;
+        const int row0 = I.q0 + quad * 32;
+        uint16_t* obase = p.dq + ((size_t)I.bh * p.N + (size_t)row0) * p.hd;
+        uint8_t* epi = gbase + C::OFF_EPI + quad * 2048;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t rr[32];
-          tmem_ld_32x32b_x32(trow + C::T_DQ + c0, rr);
+          uint32_t rv[32];
+          tmem_ld_32x32b_x32(trow + C::T_DQ + c0, rv);
           tmem_wait_ld();
-          reg_fence<32>(rr);
+          reg_fence<32>(rv);
           uint32_t pk[16];
 #pragma unroll
           for (int e = 0; e < 32; e += 2)
-            pk[e >> 1] = pack_bf16(__uint_as_float(rr[e]) * p.scale, __uint_as_float(rr[e + 1]) * p.scale);
-          if (store) {
-            uint4* o4 = reinterpret_cast<uint4*>(dst + c0);
+            pk[e >> 1] = pack_bf16(__uint_as_float(rv[e]) * p.scale, __uint_as_float(rv[e + 1]) * p.scale);
+          if constexpr (C::EPI_BYTES > 0) {
+            // Staged: each warp store covers 8 rows x 64 contiguous bytes.
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              if (c0 + 8 * v < p.hd) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            for (int u = 0; u < 4; ++u)
+              *reinterpret_cast<uint4*>(epi + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) =
+                  make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int ri = jj * 8 + (lane >> 2), u = lane & 3;
+              const uint4 val = *reinterpret_cast<const uint4*>(epi + ri * 64 + ((u ^ ((ri >> 1) & 3)) << 4));
+              if (row0 + ri < p.N && c0 + 8 * u < p.hd)
+                *reinterpret_cast<uint4*>(obase + (size_t)ri * p.hd + c0 + 8 * u) = val;
+            }
+            __syncwarp();
+          } else {
+            if (qi < p.N) {
+              uint4* o4 = reinterpret_cast<uint4*>(obase + (size_t)lane * p.hd + c0);
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                if (c0 + 8 * v < p.hd) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
           }
         }
+        tc_fence_before();
       }
     }
   }

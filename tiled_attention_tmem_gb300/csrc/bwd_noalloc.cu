@@ -106,7 +106,8 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   kp.scale_log2 = scale * kLog2e;
   kp.scale = scale;
   kp.causal = causal;
-  kp.group = causal ? l2_head_group(N, D, BH) : head_group(((N + KV::BN - 1) / KV::BN) * KV::DSPLIT, BH);
+  kp.group = causal ? l2_head_group(N, D, BH, ((N + KV::BN - 1) / KV::BN) * KV::DSPLIT)
+                    : head_group(((N + KV::BN - 1) / KV::BN) * KV::DSPLIT, BH);
   kp.sched = sched;
   const long long kv_items = (long long)((N + KV::BN - 1) / KV::BN) * BH * KV::DSPLIT;
   if (kv_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
@@ -139,9 +140,13 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   qp.scale_log2 = scale * kLog2e;
   qp.scale = scale;
   qp.causal = causal;
-  qp.group = causal ? BH : head_group((N + 127) / 128, BH);
-  const long long q_blocks = (long long)((N + 127) / 128) * BH;
-  return launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<Q7>, dim3((unsigned)q_blocks), dim3(Q7::THREADS), Q7::SMEM_BYTES,
+  qp.group = causal ? l2_head_group(N, D, BH, (N + 127) / 128) : head_group((N + 127) / 128, BH);
+  qp.sched = sched;
+  const long long q_items = (long long)((N + 127) / 128) * BH;
+  if (q_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
+  qp.items = (int)q_items;
+  const long long q_grid = std::min<long long>(q_items, sm_count_cached());
+  return launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<Q7>, dim3((unsigned)q_grid), dim3(Q7::THREADS), Q7::SMEM_BYTES,
                 st, qp);
 }
 

@@ -2,6 +2,7 @@
 // variant choice, and dispatch to the kernel launchers.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -85,14 +86,20 @@ int head_group(int tiles_per_head, int BH) {
   return g < 1 ? 1 : (g > BH ? BH : g);
 }
 
-int l2_head_group(int N, int d, int BH) {
+int l2_head_group(int N, int d, int BH, int tiles_per_head) {
   // Q, K, V, dO (bf16) and the fp32 dQ accumulator of one head; about 96 MiB
-  // of them in flight stays well inside L2 next to the other traffic.
+  // of them in flight stays well inside L2 next to the other traffic.  A group
+  // keeps at least three waves of work items, so that balancing heaviest-first
+  // inside it still has room (measured: fewer items per group lost more to the
+  // imbalance than L2 reuse gained).
   const double per_head = 12.0 * (double)N * (double)d;
-  const double g = per_head > 0 ? (96.0 * 1024 * 1024) / per_head : (double)BH;
+  double g = per_head > 0 ? (96.0 * 1024 * 1024) / per_head : (double)BH;
+  const int t = tiles_per_head > 0 ? tiles_per_head : 1;
+  g = std::max(g, std::ceil(3.0 * sm_count_cached() / t));
   const int gi = g < 1.0 ? 1 : (g > (double)BH ? BH : (int)g);
-  // Equal-sized groups: a small last group would start its heaviest items last.
-  const int ngroups = (BH + gi - 1) / gi;
+  // Equal-sized groups of at least gi heads: a small last group would start its
+  // heaviest items last.
+  const int ngroups = std::max(1, BH / gi);
   return (BH + ngroups - 1) / ngroups;
 }
 

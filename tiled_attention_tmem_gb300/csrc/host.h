@@ -28,7 +28,7 @@ int head_group(int tiles_per_head, int BH);
 // Heads per launch-order group so that their backward operands (Q, K, V, dO
 // and the fp32 dQ accumulator) fit in L2; for kernels that claim work items
 // dynamically, which keeps the balance of heaviest-first inside each group.
-int l2_head_group(int N, int d, int BH);
+int l2_head_group(int N, int d, int BH, int tiles_per_head);
 
 // Multiprocessor count of the current device (cached per device).
 int sm_count_cached();
