@@ -39,8 +39,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum).  Keyed by the workload and the
 # hash of the kernel sources it was taken on; any source change voids it.
 NCU_TRAFFIC = {
-    ("b4_h16_n2048_d128_causal", "bwd_kv5", "37fbcfcfd69a5f20"): 312.1e6,
-    ("b4_h16_n2048_d128_causal", "fwd", "37fbcfcfd69a5f20"): 154.4e6,
+    ("b4_h16_n2048_d128_causal", "bwd_kv5", "951163da608ee5d3"): 311.1e6,
+    ("b4_h16_n2048_d128_causal", "fwd", "951163da608ee5d3"): 154.5e6,
 }
 
 
