@@ -130,3 +130,26 @@ def test_no_cpu_fallback_when_library_missing(tmp_path, monkeypatch):
     monkeypatch.setattr(b, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         b.fa_fwd(A, A, A, A, A, 1, 1, 128, 64, 0.125, 0, None)
+
+
+def test_bwd_noalloc_validation(lib):
+    """Argument checks of the allocation-free backward (none of these launch anything)."""
+    def call(B=1, H=2, N=128, d=64, scale=0.125, causal=0, variant=b.FA_BWD_7GEMM, q=A, dq=A):
+        return b.fa_bwd_noalloc(q, A, A, A, A, A, dq, A, A, B, H, N, d, scale, causal, variant, None)
+
+    assert call(variant=3) == b.FA_ERR_INVALID_ARG
+    assert call(scale=0.0) == b.FA_ERR_INVALID_ARG
+    assert call(causal=2) == b.FA_ERR_INVALID_ARG
+    assert call(B=-1) == b.FA_ERR_INVALID_ARG
+    assert call(d=80) == b.FA_ERR_UNSUPPORTED
+    assert call(d=160) == b.FA_ERR_UNSUPPORTED
+    assert call(q=0) == b.FA_ERR_INVALID_ARG
+    assert call(dq=A + 2) == b.FA_ERR_MISALIGNED
+    assert call(N=0) == b.FA_OK  # empty problem: no-op
+    # head dims above 128 have no 5-GEMM kernel
+    assert call(d=256, variant=b.FA_BWD_5GEMM) == b.FA_ERR_UNSUPPORTED
+    assert call(d=192, variant=b.FA_BWD_5GEMM) == b.FA_ERR_UNSUPPORTED
+    # scratch beyond the static array is refused before anything is launched
+    big = dict(B=64, H=64, N=8192)
+    assert call(d=128, variant=b.FA_BWD_7GEMM, **big) == b.FA_ERR_WORKSPACE
+    assert call(d=128, variant=b.FA_BWD_5GEMM, **big) == b.FA_ERR_WORKSPACE

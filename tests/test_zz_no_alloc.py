@@ -25,6 +25,9 @@ CASES = [
     (1, 2, 384, 128, True, b.FA_BWD_7GEMM),
     (2, 2, 200, 64, False, b.FA_BWD_AUTO),
     (1, 2, 256, 256, True, b.FA_BWD_7GEMM),
+    # head dims run on zero-padded tiles
+    (1, 2, 300, 96, True, b.FA_BWD_5GEMM),
+    (1, 2, 200, 192, False, b.FA_BWD_AUTO),
 ]
 
 
