@@ -329,6 +329,24 @@ def run_ours(args, rank, world, local_rank):
                  "fwd_frac": fwd_tf / exp_fwd_tf if fwd_tf else None,
                  "bwd_frac": bwd_tf / exp_bwd_tf if bwd_tf else None}
 
+    # The HBM-bound helper kernels against the measured copy bandwidth:
+    # algorithmic bytes per launch / average launch time.
+    npad = (w.N + 127) // 128 * 128
+    dk_ = 64 if w.d <= 64 else (128 if w.d <= 128 else 256)  # kernel head dim (96 -> 128)
+    bh = w.B * w.H
+    hbm_bytes = {
+        # O, dO and LSE read; log2-domain LSE and D written; 5-GEMM: fp32 dQ accumulator zeroed
+        "bwd_pre": 2 * bh * w.N * w.d * 2 + 4 * bh * w.N + 8 * bh * npad
+        + (4 * bh * npad * dk_ if chosen == b.FA_BWD_5GEMM else 0),
+        # fp32 dQ accumulator read, bf16 dQ written
+        "bwd_conv": 4 * bh * w.N * dk_ + 2 * bh * w.N * w.d,
+    }
+    hbm = {}
+    for name_, bytes_ in hbm_bytes.items():
+        if name_ in kernels:
+            gbs = bytes_ / (kernels[name_]["ms_avg"] / 1e3) / 1e9
+            hbm[name_] = {"bytes": bytes_, "GB/s": gbs, "frac": gbs / float(peaks["hbm_gbs"])}
+
     # End to end through the public API: every step copies its Q, K, V, dO from
     # pinned host memory to the device and its O, LSE, dQ, dK, dV back to pinned
     # host memory.  Steps are pipelined over two sets of device buffers and three
@@ -414,7 +432,7 @@ def run_ours(args, rank, world, local_rank):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
             "frac_of_peak": frac, "peak_tflops": float(peaks["bf16_tflops"]),
-            "roofline": roof, "exp_bound": exp_bound, "cpu_baseline": cpu,
+            "roofline": roof, "exp_bound": exp_bound, "hbm_kernels": hbm, "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps,
                     "pipelining": "copy in / compute / copy out on three streams, two device buffer sets"},
