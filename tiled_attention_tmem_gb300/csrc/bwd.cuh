@@ -148,8 +148,8 @@ __global__ void __launch_bounds__(256) bwd_conv_kernel(const ConvParams p) {
 //   dK  += dS^T Q    (A = dS^T from TMEM, B = Q MN-major)
 //   5-GEMM, d = 128: dQ^T = K^T dS^T (A = K MN-major, B = dS^T smem MN-major),
 //                    lanes = d;  d = 64: dQ = dS K (A = dS^T smem MN-major,
-//                    B = K MN-major), lanes = query.  Drained by warps 8..11
-//                    through shared memory into bulk fp32 reductions.
+//                    B = K MN-major), lanes = query.  Drained by the last
+//                    warpgroup through shared memory into bulk fp32 reductions.
 //
 // SEP: P^T and dS^T get their own TMEM columns, so S^T(i+1) and dP^T(i+1) are
 // issued before dV(i), dK(i), dQ(i) and overlap the softmax of tile i+1.
