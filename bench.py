@@ -39,8 +39,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum).  Keyed by the workload and the
 # hash of the kernel sources it was taken on; any source change voids it.
 NCU_TRAFFIC = {
-    ("b4_h16_n2048_d128_causal", "bwd_kv5", "951163da608ee5d3"): 311.1e6,
-    ("b4_h16_n2048_d128_causal", "fwd", "951163da608ee5d3"): 154.5e6,
+    ("b4_h16_n2048_d128_causal", "bwd_kv5", "34e610f579233b02"): 311.1e6,
+    ("b4_h16_n2048_d128_causal", "fwd", "34e610f579233b02"): 154.5e6,
 }
 
 
@@ -58,11 +58,18 @@ def parse_args():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the CUDA sources with // comments and blank lines removed, so that a
+    change to comments alone keeps the recorded ncu traffic valid."""
     d = os.path.join(ROOT, "tiled_attention_tmem_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            code = []
+            for line in fh:
+                s = line.split("//", 1)[0].rstrip()
+                if s:
+                    code.append(s)
+        h.update(f.encode() + "\n".join(code).encode())
     return h.hexdigest()[:16]
 
 
