@@ -15,7 +15,7 @@ using KV5_64 = BwdKVCfg<64, 128, true, 1, 2, false>;
 using KV5_128 = BwdKVCfg<128, 64, true, 1, 3, true>;
 using KV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
 using KV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
-using KV7_256 = BwdKVCfg<256, 64, false, 2, 1, false>;
+using KV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true>;
 // dQ kernel configurations <d, keys per tile, K/V ring slots>.
 using Q7_64 = BwdQCfg<64, 128, 6>;
 using Q7_128 = BwdQCfg<128, 128, 4>;
@@ -81,6 +81,7 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
   p.dqacc = w.dqacc;
   p.dk = static_cast<uint16_t*>(dk);
   p.dv = static_cast<uint16_t*>(dv);
+  p.v = static_cast<const uint16_t*>(v);
   p.err = device_error_word();
   if (!p.err) return record_cuda_error(cudaErrorMemoryAllocation);
   p.N = N;

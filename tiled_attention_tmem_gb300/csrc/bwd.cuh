@@ -154,11 +154,15 @@ __global__ void __launch_bounds__(256) bwd_conv_kernel(const ConvParams p) {
 // SEP: P^T and dS^T get their own TMEM columns, so S^T(i+1) and dP^T(i+1) are
 // issued before dV(i), dK(i), dQ(i) and overlap the softmax of tile i+1.
 // Otherwise they alias the S^T / dP^T columns and the MMA order is sequential.
+// VT: V lives in TMEM (written by the compute warps, thread = key row) and
+// dP^T = V dO^T takes A from TMEM; the 64 KB of shared memory this saves at
+// d = 256 holds a second query stage.
 struct BwdKVParams {
   CUtensorMap q_map;   // box {64, BM, 1}
   CUtensorMap k_map;   // box {64, 128, 1}
   CUtensorMap v_map;   // box {64, 128, 1}
   CUtensorMap do_map;  // box {64, BM, 1}
+  const uint16_t* v;   // bf16 [BH, N, hd] (read row by row into TMEM by VT configurations)
   const float* lse2;
   const float* dd;
   float* dqacc;
@@ -175,10 +179,10 @@ struct BwdKVParams {
   int* sched; // next unclaimed work item (zero at launch)
 };
 
-template <int D_, int BM_, bool DQ_, int DSPLIT_, int QS_, bool SEP_>
+template <int D_, int BM_, bool DQ_, int DSPLIT_, int QS_, bool SEP_, bool VT_ = false>
 struct BwdKVCfg {
   static constexpr int D = D_, BM = BM_, DSPLIT = DSPLIT_, QS = QS_;
-  static constexpr bool DQ = DQ_, SEP = SEP_;
+  static constexpr bool DQ = DQ_, SEP = SEP_, VT = VT_;
   // EARLY: the compute warps load all of S^T / dP^T into registers and release
   // those TMEM columns at once, so S^T(i+1), dP^T(i+1) run during the softmax of i.
   static constexpr bool EARLY = SEP && BM == 64;
@@ -203,7 +207,7 @@ struct BwdKVCfg {
   static constexpr uint32_t STAGE_BYTES = (STAGE_TX + 1023) / 1024 * 1024;
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + KV_TILE;
-  static constexpr uint32_t OFF_STAGE = OFF_V + KV_TILE;  // Q, dO, lse2, dd per stage
+  static constexpr uint32_t OFF_STAGE = OFF_V + (VT ? 0 : KV_TILE);  // Q, dO, lse2, dd per stage
   static constexpr uint32_t OFF_DS = OFF_STAGE + QS * STAGE_BYTES;
   static constexpr uint32_t OFF_STG = OFF_DS + (DQ ? DS_TILE : 0);
   // Shared-memory staging for the bulk dQ reductions (one query tile of fp32).
@@ -213,7 +217,8 @@ struct BwdKVCfg {
                        B_PDS = B_SDP + 1, B_MMA = B_PDS + 1, B_DQFULL = B_MMA + 1,
                        B_DQFREE = B_DQFULL + 1, B_STGFREE = B_DQFREE + 1, B_STGFULL = B_STGFREE + 1,
                        B_SCONS = B_STGFULL + 1, B_DONE = B_SCONS + 1, B_KVEMPTY = B_DONE + 1,
-                       B_ITEMFULL = B_KVEMPTY + 1, B_ITEMEMPTY = B_ITEMFULL + 4, NBAR = B_ITEMEMPTY + 4;
+                       B_ITEMFULL = B_KVEMPTY + 1, B_ITEMEMPTY = B_ITEMFULL + 4, B_VREADY = B_ITEMEMPTY + 4,
+                       NBAR = B_VREADY + 1;
   static constexpr int IQ = 4;  // claimed work items passed from the producer to the other roles
   // Roles that read each work item: the MMA issuing thread(s), the compute warps, the drain warps.
   static constexpr int ITEM_READERS = (EARLY ? 2 : 1) + 4 * NCW + (DQ ? 4 : 0);
@@ -226,7 +231,8 @@ struct BwdKVCfg {
   static constexpr int T_ACC = SEP ? 3 * BM : 2 * BM;
   static constexpr int T_DV = T_ACC, T_DK = T_ACC + DH, T_DQ = T_ACC + 2 * DH;
   static constexpr int DQ_COLS = DQ ? (DQ_T ? BM : D) : 0;
-  static constexpr int TMEM_USED = T_DQ + DQ_COLS;
+  static constexpr int T_V = T_DQ + DQ_COLS;  // VT: V as packed bf16 pairs, D / 2 columns
+  static constexpr int TMEM_USED = T_V + (VT ? D / 2 : 0);
   static constexpr uint32_t TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
   static constexpr int THREADS = 128 * (1 + NCW + (DQ ? 1 : 0));
   // setmaxnreg budgets per warpgroup (producer/MMA, compute, dQ drain): the sum
@@ -244,6 +250,7 @@ struct BwdKVCfg {
   static_assert(!DQ || DSPLIT == 1, "5-GEMM keeps all of dQ's columns");
   static_assert(!DQ || D == 64 ? true : (D == 128 && BM == 64), "dQ^T path needs M = d = 128");
   static_assert(!(DQ && D == 64) || BM == 128, "dQ path needs M = BM = 128");
+  static_assert(!VT || (!EARLY && NCW == 1), "V in TMEM is written by the single compute warpgroup");
 };
 
 template <class C>
@@ -284,6 +291,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
     mbar_init(BAR(C::B_STGFULL), 4);
     mbar_init(BAR(C::B_SCONS), 4 * C::NCW);
     mbar_init(BAR(C::B_DONE), C::EARLY ? 2 : 1);
+    mbar_init(BAR(C::B_VREADY), 4 * C::NCW);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -417,10 +425,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           for (; ok && i < pre; ++i) ok = issue_stage(i);
           if (!ok) break;
           if (nkv > 0 && !wait_one(BAR(C::B_KVEMPTY), (nkv - 1) & 1, ab, (kKBwdKV << 8) | 15)) break;
-          mbar_expect_tx(BAR(C::B_KV), 2 * C::KV_TILE);
+          mbar_expect_tx(BAR(C::B_KV), (C::VT ? 1 : 2) * C::KV_TILE);
           for (int pn = 0; pn < C::PANELS; ++pn) {
             tma_load_3d(sbase + C::OFF_K + pn * C::KV_PANEL, &p.k_map, BAR(C::B_KV), 64 * pn, I.k0, I.bh);
-            tma_load_3d(sbase + C::OFF_V + pn * C::KV_PANEL, &p.v_map, BAR(C::B_KV), 64 * pn, I.k0, I.bh);
+            if (!C::VT)
+              tma_load_3d(sbase + C::OFF_V + pn * C::KV_PANEL, &p.v_map, BAR(C::B_KV), 64 * pn, I.k0, I.bh);
           }
           ++nkv;
           if (has_next)
@@ -448,16 +457,30 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         constexpr uint32_t idS = make_idesc(128, BM, false, false);
         constexpr uint32_t idAcc = make_idesc(128, DH, false, true);
         const uint32_t kt = sbase + C::OFF_K, vt = sbase + C::OFF_V;
-        auto issue_sdp = [&](int s) {
+        auto issue_s = [&](int s) {
 #pragma unroll
           for (int k = 0; k < D / 16; ++k)
             mma_ss(tmem + C::T_ST, desc_kmajor(kt, C::KV_PANEL, 16 * k),
                    desc_kmajor(stage_q(s), C::QD_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+        };
+        auto issue_dp = [&](int s) {
+          if constexpr (C::VT) {
+            // A = V from TMEM: 16 keys' worth of d per MMA is 8 packed columns.
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k)
-            mma_ss(tmem + C::T_DPT, desc_kmajor(vt, C::KV_PANEL, 16 * k),
-                   desc_kmajor(stage_do(s), C::QD_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+            for (int k = 0; k < D / 16; ++k)
+              mma_ts(tmem + C::T_DPT, tmem + C::T_V + 8 * k, desc_kmajor(stage_do(s), C::QD_PANEL, 16 * k), idS,
+                     k > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              mma_ss(tmem + C::T_DPT, desc_kmajor(vt, C::KV_PANEL, 16 * k),
+                     desc_kmajor(stage_do(s), C::QD_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+          }
           mma_commit(BAR(C::B_SDP));
+        };
+        auto issue_sdp = [&](int s) {
+          issue_s(s);
+          issue_dp(s);
         };
         auto issue_acc = [&](int s, int h, bool first) {
           const uint32_t dob = stage_do(s) + h * (DH / 64) * C::QD_PANEL;
@@ -558,7 +581,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
                 !wait_warp(BAR(C::B_QDFULL + g % QS), (g / QS) & 1, ab, (kKBwdKV << 8) | 3))
               break;
             tc_fence_after();
-            issue_sdp(g % QS);
+            issue_s(g % QS);
+            // VT: the compute warps have written this item's V into TMEM.
+            if (C::VT && !wait_warp(BAR(C::B_VREADY), nkv & 1, ab, (kKBwdKV << 8) | 19)) break;
+            tc_fence_after();
+            issue_dp(g % QS);
             for (int i = 0; i < I.n; ++i, ++g) {
               const int s = g % QS;
               const int s1 = (g + 1) % QS;
@@ -627,6 +654,31 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
               }
             }
           continue;
+        }
+        if constexpr (C::VT) {
+          // This item's V row kj as packed bf16 pairs into TMEM lane r: the A
+          // operand of dP^T = V dO^T.  The previous item's dP^T MMAs, the last
+          // readers of these columns, completed before its last S^T / dP^T
+          // barrier, which these warps have waited on.
+          const uint16_t* vrow = p.v + ((size_t)I.bh * p.N + (key_ok ? kj : 0)) * p.hd;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 64) {
+            uint32_t vw[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              uint4 x = make_uint4(0u, 0u, 0u, 0u);
+              if (key_ok && c0 + 8 * u < p.hd) x = *reinterpret_cast<const uint4*>(vrow + c0 + 8 * u);
+              vw[4 * u] = x.x;
+              vw[4 * u + 1] = x.y;
+              vw[4 * u + 2] = x.z;
+              vw[4 * u + 3] = x.w;
+            }
+            tmem_st_32x32b_x32(trow + C::T_V + (c0 >> 1), vw);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(C::B_VREADY));
         }
         for (int i = 0; i < I.n; ++i, ++g) {
           const int s = g % QS;

@@ -98,6 +98,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   kp.dqacc = dqacc;
   kp.dk = static_cast<uint16_t*>(dk);
   kp.dv = static_cast<uint16_t*>(dv);
+  kp.v = static_cast<const uint16_t*>(v);
   kp.err = err;
   kp.N = N;
   kp.Npad = Npad;
@@ -155,7 +156,7 @@ using NKV5_64 = BwdKVCfg<64, 128, true, 1, 2, false>;
 using NKV5_128 = BwdKVCfg<128, 64, true, 1, 3, true>;
 using NKV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
 using NKV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
-using NKV7_256 = BwdKVCfg<256, 64, false, 2, 1, false>;
+using NKV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true>;
 using NQ7_64 = BwdQCfg<64, 128, 6>;
 using NQ7_128 = BwdQCfg<128, 128, 4>;
 using NQ7_256 = BwdQCfg<256, 64, 3>;

@@ -13,7 +13,8 @@
 // CTA = NQ query tiles of 128 rows sharing one stream of K/V tiles (BN keys).
 //   warp 0        TMA producer: Q tiles once, then K_j, V_j through a ring of
 //                 STAGES shared-memory slots (mbarrier full/empty pairs)
-//   warp 1        TMEM allocator and single-thread tcgen05.mma issuer:
+//   warp 1        TMEM allocator and tcgen05.mma issuer (the whole warp runs
+//                 the loop, one elected lane issues):
 //                 S_t = Q_t K_j^T (both K-major, smem x smem -> TMEM) and
 //                 O_t += P_t V_j (P from TMEM, V MN-major from smem)
 //   warps 4..     one warpgroup per query tile; thread r owns row r of the tile
