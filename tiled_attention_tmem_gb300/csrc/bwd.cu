@@ -19,7 +19,7 @@ using KV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true>;
 // dQ kernel configurations <d, keys per tile, K/V ring slots>.
 using Q7_64 = BwdQCfg<64, 128, 6>;
 using Q7_128 = BwdQCfg<128, 128, 4>;
-using Q7_256 = BwdQCfg<256, 64, 3>;
+using Q7_256 = BwdQCfg<256, 64, 5, true>;
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -117,6 +117,7 @@ fa_status run_q(const void* q, const void* k, const void* v, const void* dO, con
   p.lse2 = w.lse2;
   p.dd = w.dd;
   p.dq = static_cast<uint16_t*>(dq);
+  p.dO = static_cast<const uint16_t*>(dO);
   p.err = device_error_word();
   if (!p.err) return record_cuda_error(cudaErrorMemoryAllocation);
   p.N = N;

@@ -954,6 +954,7 @@ struct BwdQParams {
   CUtensorMap do_map;  // box {64, 128, 1}
   CUtensorMap k_map;   // box {64, BN, 1}
   CUtensorMap v_map;   // box {64, BN, 1}
+  const uint16_t* dO;  // bf16 [BH, N, hd] (read row by row into TMEM by DT configurations)
   const float* lse2;
   const float* dd;
   uint16_t* dq;
@@ -968,15 +969,20 @@ struct BwdQParams {
   int* sched;  // [1]: next unclaimed work item (zero at launch)
 };
 
-template <int D_, int BN_, int STAGES_>
+// DT: dO lives in TMEM (written by the compute warps, thread = query row) and
+// dP = dO V^T takes A from TMEM; the shared memory this saves holds more K/V
+// slots, and the MMA order becomes S(j+1) (once the compute warps hold S(j) in
+// registers), dQ(j), dP(j+1), so that S(j+1) runs during the softmax of j.
+template <int D_, int BN_, int STAGES_, bool DT_ = false>
 struct BwdQCfg {
   static constexpr int D = D_, BN = BN_, STAGES = STAGES_;
+  static constexpr bool DT = DT_;
   static constexpr int PANELS = D / 64;
   static constexpr uint32_t Q_PANEL = 128 * 128;
   static constexpr uint32_t Q_TILE = PANELS * Q_PANEL;
   static constexpr uint32_t KV_PANEL = BN * 128;
   static constexpr uint32_t KV_TILE = PANELS * KV_PANEL;
-  static constexpr uint32_t OFF_Q = 0, OFF_DO = Q_TILE, OFF_KV = 2 * Q_TILE;
+  static constexpr uint32_t OFF_Q = 0, OFF_DO = Q_TILE, OFF_KV = (DT ? 1 : 2) * Q_TILE;
   static constexpr uint32_t OFF_EPI = OFF_KV + STAGES * KV_TILE;
   // dQ epilogue staging (2 KB per compute warp) where shared memory allows.
   static constexpr uint32_t EPI_BYTES = OFF_EPI + 4 * 2048 + 512 + 1024 <= 232448 ? 4 * 2048 : 0;
@@ -984,15 +990,18 @@ struct BwdQCfg {
   static constexpr int IQ = 4;  // claimed work items passed from the producer to the other roles
   static constexpr int B_QFULL = 0, B_QEMPTY = 1, B_KVFULL = 2, B_KVEMPTY = 2 + STAGES, B_SDP = 2 + 2 * STAGES,
                        B_DS = B_SDP + 1, B_DQ = B_DS + 1, B_DONE = B_DQ + 1, B_ITEMFULL = B_DONE + 1,
-                       B_ITEMEMPTY = B_ITEMFULL + IQ, NBAR = B_ITEMEMPTY + IQ;
+                       B_ITEMEMPTY = B_ITEMFULL + IQ, B_SCONS = B_ITEMEMPTY + IQ, B_DOREADY = B_SCONS + 1,
+                       NBAR = B_DOREADY + 1;
   static constexpr int ITEM_READERS = 1 + 4;  // the MMA warp and the four compute warps
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 32 + 1024;
   static constexpr int T_S = 0, T_DP = BN, T_DQ = 2 * BN;
-  static constexpr int TMEM_USED = 2 * BN + D;
+  static constexpr int T_DO = 2 * BN + D;  // DT: dO as packed bf16 pairs, D / 2 columns
+  static constexpr int TMEM_USED = 2 * BN + D + (DT ? D / 2 : 0);
   static constexpr uint32_t TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
   static constexpr int THREADS = 256;
   static_assert(TMEM_USED <= 512 && SMEM_BYTES <= 232448, "budgets");
+  static_assert(!DT || BN <= 64, "DT holds a whole S and dP row of the tile in registers");
 };
 
 template <class C>
@@ -1026,6 +1035,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
       mbar_init(BAR(C::B_ITEMFULL + k), 1);
       mbar_init(BAR(C::B_ITEMEMPTY + k), C::ITEM_READERS);
     }
+    mbar_init(BAR(C::B_SCONS), 4);
+    mbar_init(BAR(C::B_DOREADY), 4);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -1096,10 +1107,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
           if (!publish(wn)) break;
           // The previous item's last S / dP MMAs must be done reading Q and dO.
           if (nitems > 0 && !wait_one(BAR(C::B_QEMPTY), (nitems - 1) & 1, ab, (kKBwdQ << 8) | 10)) break;
-          mbar_expect_tx(BAR(C::B_QFULL), 2 * C::Q_TILE);
+          mbar_expect_tx(BAR(C::B_QFULL), (C::DT ? 1 : 2) * C::Q_TILE);
           for (int pn = 0; pn < C::PANELS; ++pn) {
             tma_load_3d(sbase + C::OFF_Q + pn * C::Q_PANEL, &p.q_map, BAR(C::B_QFULL), 64 * pn, I.q0, I.bh);
-            tma_load_3d(sbase + C::OFF_DO + pn * C::Q_PANEL, &p.do_map, BAR(C::B_QFULL), 64 * pn, I.q0, I.bh);
+            if (!C::DT)
+              tma_load_3d(sbase + C::OFF_DO + pn * C::Q_PANEL, &p.do_map, BAR(C::B_QFULL), 64 * pn, I.q0, I.bh);
           }
           ++nitems;
           for (int j = 0; j < I.n && ok; ++j) {
@@ -1130,6 +1142,79 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
       constexpr uint32_t idQ = make_idesc(128, D, false, true);
       bool ok = true;
       int it = 0, gj = 0, nitems = 0;
+      if constexpr (C::DT) {
+        auto kv_at = [&](int s) { return sbase + C::OFF_KV + s * C::KV_TILE; };
+        // Next K or V slot in load order; false if the wait gave up.
+        auto take = [&](int& slot) -> bool {
+          slot = it % S;
+          const bool got = wait_warp(BAR(C::B_KVFULL + slot), (it / S) & 1, ab, (kKBwdQ << 8) | 3);
+          ++it;
+          return got;
+        };
+        auto issue_s = [&](int sk) {
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ss(tmem + C::T_S, desc_kmajor(sbase + C::OFF_Q, C::Q_PANEL, 16 * k),
+                   desc_kmajor(kv_at(sk), C::KV_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+        };
+        // dP = dO V^T with dO from TMEM (8 packed columns per 16 elements of d),
+        // then the commits for the compute warps and for V's slot.
+        auto issue_dp = [&](int sv) {
+#pragma unroll
+          for (int k = 0; k < D / 16; ++k)
+            mma_ts(tmem + C::T_DP, tmem + C::T_DO + 8 * k, desc_kmajor(kv_at(sv), C::KV_PANEL, 16 * k), idS,
+                   k > 0 ? 1u : 0u);
+          mma_commit(BAR(C::B_SDP));
+          mma_commit(BAR(C::B_KVEMPTY + sv));
+        };
+        for (int r = 0; ok; ++r) {
+          const int w = item_warp(r);
+          if (w < 0 || w >= p.items) break;
+          const Item I = coords(w);
+          if (!wait_warp(BAR(C::B_QFULL), nitems & 1, ab, (kKBwdQ << 8) | 2)) break;
+          ++nitems;
+          int sk = 0, sv = 0;
+          // S(0) overwrites the previous item's last S, which the compute warps
+          // have read once they arrive on SCONS for it.
+          if (!take(sk) || !take(sv) ||
+              (gj > 0 && !wait_warp(BAR(C::B_SCONS), (gj - 1) & 1, ab, (kKBwdQ << 8) | 11)))
+            break;
+          tc_fence_after();
+          issue_s(sk);
+          if (I.n == 1) mma_commit(BAR(C::B_QEMPTY));  // Q no longer read
+          if (!wait_warp(BAR(C::B_DOREADY), (nitems - 1) & 1, ab, (kKBwdQ << 8) | 12)) break;
+          tc_fence_after();
+          issue_dp(sv);
+          for (int j = 0; ok && j < I.n; ++j, ++gj) {
+            const bool more = j + 1 < I.n;
+            int sk1 = 0, sv1 = 0;
+            if (more) {
+              if (!take(sk1) || !take(sv1) || !wait_warp(BAR(C::B_SCONS), gj & 1, ab, (kKBwdQ << 8) | 11)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_s(sk1);
+              if (j + 2 == I.n) mma_commit(BAR(C::B_QEMPTY));
+            }
+            if (!wait_warp(BAR(C::B_DS), gj & 1, ab, (kKBwdQ << 8) | 4)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < BN / 16; ++k)
+              mma_ts(tmem + C::T_DQ, tmem + C::T_DP + 8 * k, desc_mnmajor(kv_at(sk), C::KV_PANEL, 16 * k), idQ,
+                     (j > 0 || k > 0) ? 1u : 0u);
+            mma_commit(BAR(C::B_DQ));
+            mma_commit(BAR(C::B_KVEMPTY + sk));
+            // dP(j+1) overwrites dS(j) in dP's columns: issued after dQ(j), which reads it first.
+            if (more) issue_dp(sv1);
+            sk = sk1;
+            sv = sv1;
+          }
+        }
+      } else
       for (int r = 0; ok; ++r) {
         const int w = item_warp(r);
         if (w < 0 || w >= p.items) break;
@@ -1196,6 +1281,31 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
         const float dd = p.dd[(size_t)I.bh * p.Npad + qi];
         const float2 l22 = make_float2(l2, l2), dd2 = make_float2(dd, dd);
         const int limit = p.causal ? min(qi, p.N - 1) : p.N - 1;
+        if constexpr (C::DT) {
+          // This item's dO row qi as packed bf16 pairs into TMEM lane r: the A
+          // operand of dP = dO V^T.  The previous item's dP MMAs, the last readers
+          // of these columns, completed before its last SDP barrier, which these
+          // warps have waited on.
+          const uint16_t* drow = p.dO + ((size_t)I.bh * p.N + (qi < p.N ? qi : 0)) * p.hd;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 64) {
+            uint32_t ow[32];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              uint4 x = make_uint4(0u, 0u, 0u, 0u);
+              if (qi < p.N && c0 + 8 * u < p.hd) x = *reinterpret_cast<const uint4*>(drow + c0 + 8 * u);
+              ow[4 * u] = x.x;
+              ow[4 * u + 1] = x.y;
+              ow[4 * u + 2] = x.z;
+              ow[4 * u + 3] = x.w;
+            }
+            tmem_st_32x32b_x32(trow + C::T_DO + (c0 >> 1), ow);
+          }
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR(C::B_DOREADY));
+        }
         for (int j = 0; j < I.n; ++j, ++gj) {
           if (!wait_warp(BAR(C::B_SDP), gj & 1, ab, (kKBwdQ << 8) | 5)) {
             ok = false;
@@ -1203,14 +1313,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
           }
           tc_fence_after();
           const int kbase = j * BN;
-#pragma unroll
-          for (int c0 = 0; c0 < BN; c0 += 32) {
-            uint32_t sr[32], dr[32];
-            tmem_ld_32x32b_x32(trow + C::T_S + c0, sr);
-            tmem_ld_32x32b_x32(trow + C::T_DP + c0, dr);
-            tmem_wait_ld();
-            reg_fence<32>(sr);
-            reg_fence<32>(dr);
+          // P = exp2(S c - lse2) and dS = P (dP - D) for columns [c0, c0 + 32),
+          // packed to bf16 over the first half of dP's columns (chunk c0 -> c0 / 2).
+          auto ds_chunk = [&](int c0, const uint32_t* sr, const uint32_t* dr) {
             uint32_t pk[16];
             const bool masked = kbase + c0 + 31 > limit;
 #pragma unroll
@@ -1225,8 +1330,35 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
                   fmul2(pe, fadd2(make_float2(__uint_as_float(dr[e]), __uint_as_float(dr[e + 1])), dd2));
               pk[e >> 1] = pack_bf16(ds.x, ds.y);
             }
-            // dS (bf16) over the first half of dP's columns: chunk c0 -> columns c0/2.
             tmem_st_32x32b_x16(trow + C::T_DP + (c0 >> 1), pk);
+          };
+          if constexpr (C::DT) {
+            // All of S into registers first: S(j+1) may then be issued over it.
+            uint32_t sr[BN], dr[BN];
+#pragma unroll
+            for (int c0 = 0; c0 < BN; c0 += 32) tmem_ld_32x32b_x32(trow + C::T_S + c0, sr + c0);
+            tmem_wait_ld();
+            reg_fence<BN>(sr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(BAR(C::B_SCONS));
+#pragma unroll
+            for (int c0 = 0; c0 < BN; c0 += 32) tmem_ld_32x32b_x32(trow + C::T_DP + c0, dr + c0);
+            tmem_wait_ld();
+            reg_fence<BN>(dr);
+#pragma unroll
+            for (int c0 = 0; c0 < BN; c0 += 32) ds_chunk(c0, sr + c0, dr + c0);
+          } else {
+#pragma unroll
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+              uint32_t sr[32], dr[32];
+              tmem_ld_32x32b_x32(trow + C::T_S + c0, sr);
+              tmem_ld_32x32b_x32(trow + C::T_DP + c0, dr);
+              tmem_wait_ld();
+              reg_fence<32>(sr);
+              reg_fence<32>(dr);
+              ds_chunk(c0, sr, dr);
+            }
           }
           tmem_wait_st();
           tc_fence_before();

@@ -133,6 +133,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   qp.lse2 = lse2;
   qp.dd = dd;
   qp.dq = static_cast<uint16_t*>(dq);
+  qp.dO = static_cast<const uint16_t*>(dO);
   qp.err = err;
   qp.N = N;
   qp.Npad = Npad;
@@ -159,7 +160,7 @@ using NKV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
 using NKV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true>;
 using NQ7_64 = BwdQCfg<64, 128, 6>;
 using NQ7_128 = BwdQCfg<128, 128, 4>;
-using NQ7_256 = BwdQCfg<256, 64, 3>;
+using NQ7_256 = BwdQCfg<256, 64, 5, true>;
 
 }  // namespace
 }  // namespace fa
