@@ -16,7 +16,7 @@ namespace {
 // output columns that are not stored.
 using Fwd64 = FwdCfg<64, 2, 128, 6>;
 using Fwd128 = FwdCfg<128, 2, 128, 4>;
-using Fwd256 = FwdCfg<256, 1, 128, 2>;
+using Fwd256 = FwdCfg<256, 1, 64, 6, true>;
 
 template <class C>
 fa_status run(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N, int d,
@@ -32,6 +32,7 @@ fa_status run(const void* q, const void* k, const void* v, void* o, float* lse, 
   if ((s = make_tile_map(&p.v_map, v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, N, BH, 64, C::BN,
                          CU_TENSOR_MAP_SWIZZLE_128B)) != FA_OK)
     return s;
+  p.q = static_cast<const uint16_t*>(q);
   p.o = static_cast<uint16_t*>(o);
   p.dv = d;
   p.lse = lse;

@@ -22,6 +22,12 @@
 //                 written back as bf16 into the columns of S (tcgen05.st)
 // The MMA issue order S_0(0) S_1(0) PV_0(0) S_0(1) PV_1(0) S_1(1) ... lets the
 // tensor core work on one tile while the other tile's softmax runs.
+//
+// QT (one query tile, d = 256): Q lives in TMEM (written row by row by the
+// softmax warps) and S = Q K^T takes A from TMEM, so 64-key tiles run at the
+// full MMA rate and the shared memory holds six K/V slots; S is double-buffered
+// in TMEM and the order S(0) S(1) PV(0) S(2) PV(1) ... overlaps S(j+1) with the
+// softmax of j.  K/V tiles are loaded in that order (K one step ahead of V).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -33,6 +39,7 @@ struct FwdParams {
   CUtensorMap q_map;  // 3-D {d, N, B*H} bf16, box {64, 128, 1}, 128-byte swizzle
   CUtensorMap k_map;  // same tensor shape, box {64, BN, 1}
   CUtensorMap v_map;
+  const uint16_t* q;  // bf16 [B*H, N, d] (read row by row into TMEM by QT configurations)
   uint16_t* o;  // bf16 [B*H, N, d]
   int dv;       // head dim d of the tensors (<= the kernel's D; columns d..D-1 of the tiles read as 0)
   float* lse;   // fp32 [B*H, N]
@@ -45,9 +52,11 @@ struct FwdParams {
   int items;  // work items (query blocks x heads); the grid is persistent over them
 };
 
-template <int D_, int NQ_, int BN_, int STAGES_>
+template <int D_, int NQ_, int BN_, int STAGES_, bool QT_ = false>
 struct FwdCfg {
   static constexpr int D = D_, NQ = NQ_, BN = BN_, STAGES = STAGES_;
+  static constexpr bool QT = QT_;
+  static constexpr int SB = QT ? 2 : 1;  // S buffers per query tile
   static constexpr int BM = 128;
   static constexpr int PREFETCH = STAGES / 2 + 2;  // K/V tiles ahead for L2 prefetch
   static constexpr int PANELS = D / 64;
@@ -56,24 +65,29 @@ struct FwdCfg {
   static constexpr uint32_t KV_PANEL = BN * 128;
   static constexpr uint32_t KV_TILE = PANELS * KV_PANEL;
   static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_KV = OFF_Q + NQ * Q_TILE;
+  static constexpr uint32_t OFF_KV = OFF_Q + (QT ? 0 : NQ * Q_TILE);
   // O epilogue staging: 2 KB per softmax warp (32 rows x 32 bf16 columns).
   static constexpr uint32_t OFF_EPI = OFF_KV + STAGES * KV_TILE;
   static constexpr uint32_t OFF_BAR = OFF_EPI + NQ * 4 * 2048;
-  // barriers: q_full, kv_full[S], kv_empty[S], s_full[NQ], p_ready[NQ], o_ready[NQ], done
+  // barriers: q_full, kv_full[S], kv_empty[S], s_full[NQ*SB], p_ready[NQ*SB], o_ready[NQ*SB], done,
+  // q_empty, q_ready (QT: Q written to TMEM).  With two S buffers, PV(j) commits to o_ready of
+  // buffer j & 1: S(j+1) is issued ahead of PV(j), so one barrier for all PVs could trail a
+  // waiter by two phases, which a parity wait cannot tell apart.
   static constexpr int B_QFULL = 0, B_KVFULL = 1, B_KVEMPTY = 1 + STAGES,
-                       B_SFULL = 1 + 2 * STAGES, B_PREADY = B_SFULL + NQ,
-                       B_OREADY = B_PREADY + NQ, B_DONE = B_OREADY + NQ, B_QEMPTY = B_DONE + 1,
-                       NBAR = B_QEMPTY + 1;
+                       B_SFULL = 1 + 2 * STAGES, B_PREADY = B_SFULL + NQ * SB,
+                       B_OREADY = B_PREADY + NQ * SB, B_DONE = B_OREADY + NQ * SB, B_QEMPTY = B_DONE + 1,
+                       B_QREADY = B_QEMPTY + 1, NBAR = B_QREADY + 1;
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
-  static constexpr int TMEM_S = 0;         // S_t (and P_t aliased) at t*BN
-  static constexpr int TMEM_O = NQ * BN;   // O_t at TMEM_O + t*D
-  static constexpr int TMEM_USED = NQ * (BN + D);
+  static constexpr int TMEM_S = 0;              // S_t (and P_t aliased) at (t*SB + buffer)*BN
+  static constexpr int TMEM_O = NQ * SB * BN;   // O_t at TMEM_O + t*D
+  static constexpr int TMEM_Q = TMEM_O + NQ * D;  // QT: Q as packed bf16 pairs, D / 2 columns
+  static constexpr int TMEM_USED = TMEM_Q + (QT ? D / 2 : 0);
   static constexpr uint32_t TMEM_COLS =
       TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
   static constexpr int THREADS = 128 + 128 * NQ;
   static_assert(TMEM_USED <= 512, "TMEM budget");
+  static_assert(!QT || NQ == 1, "Q in TMEM is used with one query tile");
   static_assert(BN % 32 == 0 && BN <= 256 && D % 64 == 0 && D <= 256, "tile shape");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -114,13 +128,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
       mbar_init(bar0 + 8 * (C::B_KVFULL + s), 1);
       mbar_init(bar0 + 8 * (C::B_KVEMPTY + s), 1);
     }
-    for (int t = 0; t < NQ; ++t) {
+    for (int t = 0; t < NQ * C::SB; ++t) {
       mbar_init(bar0 + 8 * (C::B_SFULL + t), 1);
       mbar_init(bar0 + 8 * (C::B_PREADY + t), 4);
       mbar_init(bar0 + 8 * (C::B_OREADY + t), 1);
     }
     mbar_init(bar0 + 8 * C::B_DONE, 1);
     mbar_init(bar0 + 8 * C::B_QEMPTY, 1);
+    mbar_init(bar0 + 8 * C::B_QREADY, 4);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -185,6 +200,27 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           const int w = item_of(r);
           if (w >= p.items) break;
           const Item I = coords(w);
+          if constexpr (C::QT) {
+            // K(0), then K(j+1) ahead of V(j): the order in which the MMAs read them.
+            auto load = [&](const CUtensorMap* m, int j) -> bool {
+              const int s = it % S;
+              if (!wait_one(BAR(C::B_KVEMPTY + s), ((it / S) & 1) ^ 1, ab, (kKFwd << 8) | 1)) return false;
+              mbar_expect_tx(BAR(C::B_KVFULL + s), C::KV_TILE);
+              for (int pn = 0; pn < C::PANELS; ++pn)
+                tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m, BAR(C::B_KVFULL + s),
+                            64 * pn, j * BN, I.bh);
+              if (j + C::PREFETCH < I.nmax)
+                for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(m, 64 * pn, (j + C::PREFETCH) * BN, I.bh);
+              ++it;
+              return true;
+            };
+            if (I.nmax > 0) ok = load(&p.k_map, 0);
+            for (int j = 0; j < I.nmax && ok; ++j) {
+              if (j + 1 < I.nmax) ok = load(&p.k_map, j + 1);
+              if (ok) ok = load(&p.v_map, j);
+            }
+            continue;
+          }
           // The previous item's S MMAs must be done reading Q.
           if (!wait_one(BAR(C::B_QEMPTY), (nitems & 1) ^ 1, ab, (kKFwd << 8) | 10)) break;
           mbar_expect_tx(BAR(C::B_QFULL), NQ * C::Q_TILE);
@@ -237,6 +273,65 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
 #pragma unroll
         for (int t = 0; t < NQ; ++t) g[t] = 0;
         bool ok = true;
+        if constexpr (C::QT) {
+          // Next K or V slot in load order (false if the wait gave up).
+          auto take = [&](int& slot) -> bool {
+            slot = it % S;
+            const bool got = wait_warp(BAR(C::B_KVFULL + slot), (it / S) & 1, ab, (kKFwd << 8) | 3);
+            ++it;
+            return got;
+          };
+          // S into buffer b with A = Q from TMEM (8 packed columns per 16 elements of d).
+          auto issue_sq = [&](int b, int sk) {
+            const uint32_t kb = sbase + C::OFF_KV + sk * C::KV_TILE;
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k)
+              mma_ts(tmem + C::TMEM_S + b * BN, tmem + C::TMEM_Q + 8 * k, desc_kmajor(kb, C::KV_PANEL, 16 * k),
+                     idS, k > 0 ? 1u : 0u);
+            mma_commit(BAR(C::B_SFULL + b));
+            mma_commit(BAR(C::B_KVEMPTY + sk));
+          };
+          for (int r = 0; ok; ++r) {
+            const int w = item_of(r);
+            if (w >= p.items) break;
+            const Item I = coords(w);
+            const int n = I.nkv[0];
+            // The softmax warps have written this item's Q into TMEM.
+            if (!wait_warp(BAR(C::B_QREADY), nitems & 1, ab, (kKFwd << 8) | 11)) break;
+            ++nitems;
+            if (n <= 0) continue;
+            int sk = 0;
+            if (!take(sk)) break;
+            tc_fence_after();
+            issue_sq(g[0] & 1, sk);
+            for (int j = 0; ok && j < n; ++j) {
+              const int gj = g[0] + j;
+              // S(j+1) into the other buffer, whose P(j-1) was read by PV(j-1) (issued before).
+              if (j + 1 < n) {
+                if (!take(sk)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                issue_sq((gj + 1) & 1, sk);
+              }
+              int sv = 0;
+              if (!take(sv) || !wait_warp(BAR(C::B_PREADY + (gj & 1)), (gj >> 1) & 1, ab, (kKFwd << 8) | 5)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t vb = sbase + C::OFF_KV + sv * C::KV_TILE;
+#pragma unroll
+              for (int k = 0; k < BN / 16; ++k)
+                mma_ts(tmem + C::TMEM_O, tmem + C::TMEM_S + (gj & 1) * BN + 8 * k,
+                       desc_mnmajor(vb, C::KV_PANEL, 16 * k), idO, (j > 0 || k > 0) ? 1u : 0u);
+              mma_commit(BAR(C::B_OREADY + (gj & 1)));
+              mma_commit(BAR(C::B_KVEMPTY + sv));
+            }
+            g[0] += n;
+          }
+        } else
         for (int r = 0; ok; ++r) {
           const int w = item_of(r);
           if (w >= p.items) break;
@@ -314,14 +409,43 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
       const int quad = warp & 3;
       const int r = quad * 32 + lane;
       const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
-      const uint32_t tS = trow + C::TMEM_S + t * BN;
       const uint32_t tO = trow + C::TMEM_O + t * D;
       const float cs = p.scale_log2;
+      // Barrier and phase parity that signal completion of this tile's gm-th PV.
+      auto oready_bar = [&](int gm) { return C::QT ? (gm & 1) : t; };
+      auto oready_phase = [&](int gm) -> uint32_t { return C::QT ? ((gm >> 1) & 1) : (gm & 1); };
       int g = 0;  // iterations of this query tile in earlier items
       bool ok = true;
+      // QT: item wq's query row r as packed bf16 pairs into TMEM lane r (the A
+      // operand of S = Q K^T).  Called once the S MMAs of the previous item,
+      // the last readers of these columns, are known to be complete.
+      auto write_q = [&](int wq) {
+        const Item J = coords(wq);
+        const int qrow = J.q0 + r;
+        const uint16_t* qsrc = p.q + ((size_t)J.bh * p.N + (qrow < p.N ? qrow : 0)) * p.dv;
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t qw[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (qrow < p.N && c0 + 8 * u < p.dv) x = *reinterpret_cast<const uint4*>(qsrc + c0 + 8 * u);
+            qw[4 * u] = x.x;
+            qw[4 * u + 1] = x.y;
+            qw[4 * u + 2] = x.z;
+            qw[4 * u + 3] = x.w;
+          }
+          tmem_st_32x32b_x32(trow + C::TMEM_Q + (c0 >> 1), qw);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(C::B_QREADY));
+      };
       for (int rr = 0; ok; ++rr) {
         const int w = item_of(rr);
         if (w >= p.items) break;
+        if (C::QT && rr == 0) write_q(w);
         const Item I = coords(w);
         const int qi = I.q0 + 128 * t + r;
         const int n = I.nkv[t];
@@ -330,7 +454,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
         float m_used = -INFINITY;
         float l = 0.f;
         for (int j = 0; j < n; ++j) {
-          if (!wait_warp(BAR(C::B_SFULL + t), (g + j) & 1, ab, (kKFwd << 8) | 7)) {
+          // S buffer (and its barriers) of this step: per tile, or alternating (QT).
+          const int sb = C::QT ? ((g + j) & 1) : t;
+          const uint32_t sph = C::QT ? (((g + j) >> 1) & 1) : ((g + j) & 1);
+          const uint32_t tS = trow + C::TMEM_S + sb * BN;
+          if (!wait_warp(BAR(C::B_SFULL + sb), sph, ab, (kKFwd << 8) | 7)) {
             ok = false;
             break;
           }
@@ -389,7 +517,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           tmem_wait_st();
           if (j > 0 && __any_sync(0xffffffffu, need)) {
             // Rescale the running O once the MMA that last accumulated into it is done.
-            if (!wait_warp(BAR(C::B_OREADY + t), (g + j - 1) & 1, ab, (kKFwd << 8) | 8)) {
+            if (!wait_warp(BAR(C::B_OREADY + oready_bar(g + j - 1)), oready_phase(g + j - 1), ab, (kKFwd << 8) | 8)) {
               ok = false;
               break;
             }
@@ -408,10 +536,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           }
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(BAR(C::B_PREADY + t));
+          if (lane == 0) mbar_arrive(BAR(C::B_PREADY + sb));
+        }
+        if (C::QT && ok) {
+          const int wn = item_of(rr + 1);
+          if (wn < p.items) write_q(wn);
         }
         if (ok && n > 0) {
-          if (!wait_warp(BAR(C::B_OREADY + t), (g + n - 1) & 1, ab, (kKFwd << 8) | 9)) {
+          if (!wait_warp(BAR(C::B_OREADY + oready_bar(g + n - 1)), oready_phase(g + n - 1), ab, (kKFwd << 8) | 9)) {
             ok = false;
             break;
           }
