@@ -91,7 +91,7 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
-  p.group = causal ? l2_head_group(N, C::D, BH, ((N + C::BN - 1) / C::BN) * C::DSPLIT)
+  p.group = causal ? l2_head_group(12.0 * N * C::D, BH, ((N + C::BN - 1) / C::BN) * C::DSPLIT)
                    : head_group(((N + C::BN - 1) / C::BN) * C::DSPLIT, BH);
   p.sched = w.sched;
   const long long items = (long long)((N + C::BN - 1) / C::BN) * BH * C::DSPLIT;
@@ -127,7 +127,7 @@ fa_status run_q(const void* q, const void* k, const void* v, const void* dO, con
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
-  p.group = causal ? l2_head_group(N, C::D, BH, (N + 127) / 128) : head_group((N + 127) / 128, BH);
+  p.group = causal ? l2_head_group(12.0 * N * C::D, BH, (N + 127) / 128) : head_group((N + 127) / 128, BH);
   p.sched = w.sched;
   const long long items = (long long)((N + 127) / 128) * BH;
   if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;

@@ -107,7 +107,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   kp.scale_log2 = scale * kLog2e;
   kp.scale = scale;
   kp.causal = causal;
-  kp.group = causal ? l2_head_group(N, D, BH, ((N + KV::BN - 1) / KV::BN) * KV::DSPLIT)
+  kp.group = causal ? l2_head_group(12.0 * N * D, BH, ((N + KV::BN - 1) / KV::BN) * KV::DSPLIT)
                     : head_group(((N + KV::BN - 1) / KV::BN) * KV::DSPLIT, BH);
   kp.sched = sched;
   const long long kv_items = (long long)((N + KV::BN - 1) / KV::BN) * BH * KV::DSPLIT;
@@ -142,7 +142,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   qp.scale_log2 = scale * kLog2e;
   qp.scale = scale;
   qp.causal = causal;
-  qp.group = causal ? l2_head_group(N, D, BH, (N + 127) / 128) : head_group((N + 127) / 128, BH);
+  qp.group = causal ? l2_head_group(12.0 * N * D, BH, (N + 127) / 128) : head_group((N + 127) / 128, BH);
   qp.sched = sched;
   const long long q_items = (long long)((N + 127) / 128) * BH;
   if (q_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;

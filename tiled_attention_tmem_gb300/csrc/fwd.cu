@@ -43,7 +43,9 @@ fa_status run(const void* q, const void* k, const void* v, void* o, float* lse, 
   p.scale_log2 = scale * kLog2e;
   p.causal = causal;
   const int n_qblk = (N + 128 * C::NQ - 1) / (128 * C::NQ);
-  p.group = causal ? BH : head_group(n_qblk, BH);
+  // Causal: heaviest query blocks first inside groups of heads whose K and V
+  // (4 N d bytes each) stay in L2.
+  p.group = causal ? l2_head_group(4.0 * N * d, BH, n_qblk) : head_group(n_qblk, BH);
   const long long items = (long long)n_qblk * BH;
   if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.items = (int)items;

@@ -86,13 +86,12 @@ int head_group(int tiles_per_head, int BH) {
   return g < 1 ? 1 : (g > BH ? BH : g);
 }
 
-int l2_head_group(int N, int d, int BH, int tiles_per_head) {
-  // Q, K, V, dO (bf16) and the fp32 dQ accumulator of one head; about 96 MiB
-  // of them in flight stays well inside L2 next to the other traffic.  A group
-  // keeps at least three waves of work items, so that balancing heaviest-first
-  // inside it still has room (measured: fewer items per group lost more to the
-  // imbalance than L2 reuse gained).
-  const double per_head = 12.0 * (double)N * (double)d;
+int l2_head_group(double head_bytes, int BH, int tiles_per_head) {
+  // About 96 MiB of re-read operands in flight stays well inside L2 next to the
+  // other traffic.  A group keeps at least three waves of work items, so that
+  // balancing heaviest-first inside it still has room (measured: fewer items per
+  // group lost more to the imbalance than L2 reuse gained).
+  const double per_head = head_bytes;
   double g = per_head > 0 ? (96.0 * 1024 * 1024) / per_head : (double)BH;
   const int t = tiles_per_head > 0 ? tiles_per_head : 1;
   g = std::max(g, std::ceil(3.0 * sm_count_cached() / t));

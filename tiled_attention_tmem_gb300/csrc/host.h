@@ -25,10 +25,11 @@ fa_status make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType 
 // one group of all heads under the causal mask, where heaviest-tile-first
 // across every head balances better than locality helps.
 int head_group(int tiles_per_head, int BH);
-// Heads per launch-order group so that their backward operands (Q, K, V, dO
-// and the fp32 dQ accumulator) fit in L2; for kernels that claim work items
-// dynamically, which keeps the balance of heaviest-first inside each group.
-int l2_head_group(int N, int d, int BH, int tiles_per_head);
+// Heads per launch-order group so that the operands each head keeps re-reading
+// (head_bytes per head: K and V for the forward; Q, K, V, dO and the fp32 dQ
+// accumulator for the backward) fit in L2, with at least three waves of work
+// items per group so that heaviest-first ordering inside a group still balances.
+int l2_head_group(double head_bytes, int BH, int tiles_per_head);
 
 // Multiprocessor count of the current device (cached per device).
 int sm_count_cached();
