@@ -23,11 +23,12 @@
 // The MMA issue order S_0(0) S_1(0) PV_0(0) S_0(1) PV_1(0) S_1(1) ... lets the
 // tensor core work on one tile while the other tile's softmax runs.
 //
-// QT (one query tile, d = 256): Q lives in TMEM (written row by row by the
-// softmax warps) and S = Q K^T takes A from TMEM, so 64-key tiles run at the
-// full MMA rate and the shared memory holds six K/V slots; S is double-buffered
-// in TMEM and the order S(0) S(1) PV(0) S(2) PV(1) ... overlaps S(j+1) with the
-// softmax of j.  K/V tiles are loaded in that order (K one step ahead of V).
+// QT (d = 256): Q lives in TMEM (written row by row by the softmax
+// warps) and S = Q K^T takes A from TMEM, so 64-key tiles run at the full MMA
+// rate and the shared memory holds more K/V slots; each tile's S is
+// double-buffered in TMEM and the order S_t(0) S_t(1) PV_t(0) S_t(2) PV_t(1) ...
+// lets the softmax warps run from one key tile to the next without waiting for
+// S.  K/V tiles are loaded in that order (K one step ahead of V).
 #pragma once
 #include <cuda_bf16.h>
 
@@ -81,13 +82,12 @@ struct FwdCfg {
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
   static constexpr int TMEM_S = 0;              // S_t (and P_t aliased) at (t*SB + buffer)*BN
   static constexpr int TMEM_O = NQ * SB * BN;   // O_t at TMEM_O + t*D
-  static constexpr int TMEM_Q = TMEM_O + NQ * D;  // QT: Q as packed bf16 pairs, D / 2 columns
-  static constexpr int TMEM_USED = TMEM_Q + (QT ? D / 2 : 0);
+  static constexpr int TMEM_Q = TMEM_O + NQ * D;  // QT: Q_t as packed bf16 pairs at TMEM_Q + t*D/2
+  static constexpr int TMEM_USED = TMEM_Q + (QT ? NQ * D / 2 : 0);
   static constexpr uint32_t TMEM_COLS =
       TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
   static constexpr int THREADS = 128 + 128 * NQ;
   static_assert(TMEM_USED <= 512, "TMEM budget");
-  static_assert(!QT || NQ == 1, "Q in TMEM is used with one query tile");
   static_assert(BN % 32 == 0 && BN <= 256 && D % 64 == 0 && D <= 256, "tile shape");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
     }
     mbar_init(bar0 + 8 * C::B_DONE, 1);
     mbar_init(bar0 + 8 * C::B_QEMPTY, 1);
-    mbar_init(bar0 + 8 * C::B_QREADY, 4);
+    mbar_init(bar0 + 8 * C::B_QREADY, 4 * NQ);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -281,55 +281,69 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
             ++it;
             return got;
           };
-          // S into buffer b with A = Q from TMEM (8 packed columns per 16 elements of d).
-          auto issue_sq = [&](int b, int sk) {
+          // S_t into buffer b of tile t with A = Q_t from TMEM (8 packed columns per
+          // 16 elements of d).
+          auto issue_sq = [&](int t, int b, int sk) {
             const uint32_t kb = sbase + C::OFF_KV + sk * C::KV_TILE;
 #pragma unroll
             for (int k = 0; k < D / 16; ++k)
-              mma_ts(tmem + C::TMEM_S + b * BN, tmem + C::TMEM_Q + 8 * k, desc_kmajor(kb, C::KV_PANEL, 16 * k),
-                     idS, k > 0 ? 1u : 0u);
-            mma_commit(BAR(C::B_SFULL + b));
-            mma_commit(BAR(C::B_KVEMPTY + sk));
+              mma_ts(tmem + C::TMEM_S + (t * C::SB + b) * BN, tmem + C::TMEM_Q + t * (D / 2) + 8 * k,
+                     desc_kmajor(kb, C::KV_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+            mma_commit(BAR(C::B_SFULL + t * C::SB + b));
           };
           for (int r = 0; ok; ++r) {
             const int w = item_of(r);
             if (w >= p.items) break;
             const Item I = coords(w);
-            const int n = I.nkv[0];
             // The softmax warps have written this item's Q into TMEM.
             if (!wait_warp(BAR(C::B_QREADY), nitems & 1, ab, (kKFwd << 8) | 11)) break;
             ++nitems;
-            if (n <= 0) continue;
+            if (I.nmax <= 0) continue;
             int sk = 0;
             if (!take(sk)) break;
             tc_fence_after();
-            issue_sq(g[0] & 1, sk);
-            for (int j = 0; ok && j < n; ++j) {
-              const int gj = g[0] + j;
-              // S(j+1) into the other buffer, whose P(j-1) was read by PV(j-1) (issued before).
-              if (j + 1 < n) {
+            for (int t = 0; t < NQ; ++t)
+              if (I.nkv[t] > 0) issue_sq(t, g[t] & 1, sk);
+            mma_commit(BAR(C::B_KVEMPTY + sk));
+            for (int j = 0; ok && j < I.nmax; ++j) {
+              // S_t(j+1) into the other buffer of tile t, whose P_t(j-1) was read by
+              // PV_t(j-1) (issued before).
+              if (j + 1 < I.nmax) {
                 if (!take(sk)) {
                   ok = false;
                   break;
                 }
                 tc_fence_after();
-                issue_sq((gj + 1) & 1, sk);
+                for (int t = 0; t < NQ; ++t)
+                  if (j + 1 < I.nkv[t]) issue_sq(t, (g[t] + j + 1) & 1, sk);
+                mma_commit(BAR(C::B_KVEMPTY + sk));
               }
               int sv = 0;
-              if (!take(sv) || !wait_warp(BAR(C::B_PREADY + (gj & 1)), (gj >> 1) & 1, ab, (kKFwd << 8) | 5)) {
+              if (!take(sv)) {
                 ok = false;
                 break;
               }
-              tc_fence_after();
               const uint32_t vb = sbase + C::OFF_KV + sv * C::KV_TILE;
+              for (int t = 0; t < NQ && ok; ++t) {
+                if (j >= I.nkv[t]) continue;
+                const int gj = g[t] + j;
+                const int sb = t * C::SB + (gj & 1);
+                if (!wait_warp(BAR(C::B_PREADY + sb), (gj >> 1) & 1, ab, (kKFwd << 8) | 5)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
 #pragma unroll
-              for (int k = 0; k < BN / 16; ++k)
-                mma_ts(tmem + C::TMEM_O, tmem + C::TMEM_S + (gj & 1) * BN + 8 * k,
-                       desc_mnmajor(vb, C::KV_PANEL, 16 * k), idO, (j > 0 || k > 0) ? 1u : 0u);
-              mma_commit(BAR(C::B_OREADY + (gj & 1)));
+                for (int k = 0; k < BN / 16; ++k)
+                  mma_ts(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + sb * BN + 8 * k,
+                         desc_mnmajor(vb, C::KV_PANEL, 16 * k), idO, (j > 0 || k > 0) ? 1u : 0u);
+                mma_commit(BAR(C::B_OREADY + sb));
+              }
+              if (!ok) break;
               mma_commit(BAR(C::B_KVEMPTY + sv));
             }
-            g[0] += n;
+#pragma unroll
+            for (int t = 0; t < NQ; ++t) g[t] += I.nkv[t];
           }
         } else
         for (int r = 0; ok; ++r) {
@@ -412,7 +426,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
       const uint32_t tO = trow + C::TMEM_O + t * D;
       const float cs = p.scale_log2;
       // Barrier and phase parity that signal completion of this tile's gm-th PV.
-      auto oready_bar = [&](int gm) { return C::QT ? (gm & 1) : t; };
+      auto oready_bar = [&](int gm) { return C::QT ? t * C::SB + (gm & 1) : t; };
       auto oready_phase = [&](int gm) -> uint32_t { return C::QT ? ((gm >> 1) & 1) : (gm & 1); };
       int g = 0;  // iterations of this query tile in earlier items
       bool ok = true;
@@ -421,7 +435,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
       // the last readers of these columns, are known to be complete.
       auto write_q = [&](int wq) {
         const Item J = coords(wq);
-        const int qrow = J.q0 + r;
+        const int qrow = J.q0 + 128 * t + r;
         const uint16_t* qsrc = p.q + ((size_t)J.bh * p.N + (qrow < p.N ? qrow : 0)) * p.dv;
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 64) {
@@ -435,7 +449,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
             qw[4 * u + 2] = x.z;
             qw[4 * u + 3] = x.w;
           }
-          tmem_st_32x32b_x32(trow + C::TMEM_Q + (c0 >> 1), qw);
+          tmem_st_32x32b_x32(trow + C::TMEM_Q + t * (D / 2) + (c0 >> 1), qw);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -455,7 +469,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
         float l = 0.f;
         for (int j = 0; j < n; ++j) {
           // S buffer (and its barriers) of this step: per tile, or alternating (QT).
-          const int sb = C::QT ? ((g + j) & 1) : t;
+          const int sb = C::QT ? t * C::SB + ((g + j) & 1) : t;
           const uint32_t sph = C::QT ? (((g + j) >> 1) & 1) : ((g + j) & 1);
           const uint32_t tS = trow + C::TMEM_S + sb * BN;
           if (!wait_warp(BAR(C::B_SFULL + sb), sph, ab, (kKFwd << 8) | 7)) {
