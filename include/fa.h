@@ -140,6 +140,17 @@ int fa_bwd_choose(int B, int H, int N, int d, int causal);
  */
 fa_status fa_get_device_error(void* stream, int* site);
 
+/*
+ * Self-test of the in-kernel watchdog: launches one warp on `stream` that waits
+ * on a barrier nothing completes.  After the watchdog limit (4e9 SM cycles,
+ * about two seconds) the wait gives up and records FA_ERR_DEVICE_TIMEOUT with
+ * site (6 << 8) | 1 in the device error word, which fa_get_device_error then
+ * reports and clears; until then, this library's kernels on this device exit
+ * without computing.  Touches no caller memory.  Returns FA_OK if the launch
+ * succeeded, FA_ERR_LAUNCH otherwise.
+ */
+fa_status fa_watchdog_selftest(void* stream);
+
 /* The last CUDA runtime error code seen by this library on this thread. */
 int fa_last_cuda_error(void);
 

@@ -40,6 +40,7 @@ SIGNATURES = {
                             _I, _I, _I, _I, _F, _I, _I, _VP]),
     "fa_bwd_choose": (_I, [_I, _I, _I, _I, _I]),
     "fa_get_device_error": (_I, [_VP, ctypes.POINTER(_I)]),
+    "fa_watchdog_selftest": (_I, [_VP]),
     "fa_last_cuda_error": (_I, []),
     "fa_strerror": (ctypes.c_char_p, [_I]),
     "fa_profile_start": (_I, []),
@@ -113,6 +114,10 @@ def fa_get_device_error(stream) -> tuple[int, int]:
     site = _I(0)
     status = lib().fa_get_device_error(stream, ctypes.byref(site))
     return status, site.value
+
+
+def fa_watchdog_selftest(stream) -> int:
+    return lib().fa_watchdog_selftest(stream)
 
 
 def fa_last_cuda_error() -> int:

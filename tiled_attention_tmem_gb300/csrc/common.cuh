@@ -11,7 +11,7 @@ namespace fa {
 //   err[0] = status (0 = ok, 6 = a bounded wait expired)
 //   err[1] = where: (kernel id << 8) | wait site
 constexpr int kDevErrTimeout = 6;
-enum KernelId : int { kKFwd = 1, kKBwdKV = 2, kKBwdQ = 3, kKPre = 4, kKConv = 5 };
+enum KernelId : int { kKFwd = 1, kKBwdKV = 2, kKBwdQ = 3, kKPre = 4, kKConv = 5, kKSelfTest = 6 };
 
 // About two seconds at the maximum SM clock: far longer than any legitimate
 // wait inside these kernels (microseconds), short enough to keep a broken
