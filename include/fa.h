@@ -67,7 +67,7 @@ typedef enum {
 /*
  * Forward.  q, k, v: [B,H,N,d] bf16 (read).  o: [B,H,N,d] bf16 (written).
  * lse: [B,H,N] fp32 (written), natural log.  d must be 64, 96, 128, 192 or 256
- * (96 and 192 run the 128 / 256 kernels on zero-padded tiles).
+ * (96 runs the 128 kernels on zero-padded tiles; 192 has its own).
  * scale: finite and > 0 (typically 1/sqrt(d)).  causal: 0 or 1 (key j is
  * visible to query i iff j <= i).  B*H*N == 0 is a no-op returning FA_OK.
  */

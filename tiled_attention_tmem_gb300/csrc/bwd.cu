@@ -15,10 +15,13 @@ using KV5_64 = BwdKVCfg<64, 128, true, 1, 2, false>;
 using KV5_128 = BwdKVCfg<128, 64, true, 1, 3, true>;
 using KV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
 using KV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
+// d = 192: dV and dK for all 192 columns fit TMEM next to S and dP, so no d split.
+using KV7_192 = BwdKVCfg<192, 64, false, 1, 2, false>;
 using KV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true>;
 // dQ kernel configurations <d, keys per tile, K/V ring slots>.
 using Q7_64 = BwdQCfg<64, 128, 6>;
 using Q7_128 = BwdQCfg<128, 128, 4>;
+using Q7_192 = BwdQCfg<192, 64, 7, true>;
 using Q7_256 = BwdQCfg<256, 64, 5, true>;
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -159,11 +162,15 @@ fa_status run_d(const void* q, const void* k, const void* v, const void* o, cons
 
 }  // namespace
 
-// d = 96 and d = 192 run the d = 128 and d = 256 kernels on zero-padded tiles
-// (TMA reads the columns past d as zeros; nothing past d is stored).
+// d = 96 runs the d = 128 kernels on zero-padded tiles (TMA reads the columns
+// past d as zeros; nothing past d is stored).  d = 192 has its own dK/dV and dQ
+// kernels; its preprocess is the d = 256 one (which reads only d columns).
 fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, const void* dO, const float* lse,
                   void* dq, void* dk, void* dv, int BH, int N, int d, float scale, int causal, int variant,
                   void* workspace, cudaStream_t st) {
+  if (d == 192)
+    return run_d<256, void, KV7_192, Q7_192>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, variant,
+                                             workspace, st);
   switch (padded_head_dim(d)) {
     case 64:
       return run_d<64, KV5_64, KV7_64, Q7_64>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, variant,

@@ -157,9 +157,11 @@ using NKV5_64 = BwdKVCfg<64, 128, true, 1, 2, false>;
 using NKV5_128 = BwdKVCfg<128, 64, true, 1, 3, true>;
 using NKV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
 using NKV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
+using NKV7_192 = BwdKVCfg<192, 64, false, 1, 2, false>;
 using NKV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true>;
 using NQ7_64 = BwdQCfg<64, 128, 6>;
 using NQ7_128 = BwdQCfg<128, 128, 4>;
+using NQ7_192 = BwdQCfg<192, 64, 7, true>;
 using NQ7_256 = BwdQCfg<256, 64, 5, true>;
 
 }  // namespace
@@ -202,6 +204,8 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
                   : run<NKV7_128, NQ7_128, 128>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, false, base,
                                                 st);
     default:
+      if (d == 192)
+        return run<NKV7_192, NQ7_192, 256>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, false, base, st);
       return run<NKV7_256, NQ7_256, 256>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, false, base, st);
   }
 }

@@ -16,6 +16,7 @@ namespace {
 // output columns that are not stored.
 using Fwd64 = FwdCfg<64, 2, 128, 6>;
 using Fwd128 = FwdCfg<128, 2, 128, 4>;
+using Fwd192 = FwdCfg<192, 1, 64, 8, true>;
 using Fwd256 = FwdCfg<256, 1, 64, 6, true>;
 
 template <class C>
@@ -63,7 +64,7 @@ fa_status run_fwd(const void* q, const void* k, const void* v, void* o, float* l
     case 64: return run<Fwd64>(q, k, v, o, lse, BH, N, d, scale, causal, st);
     case 96:
     case 128: return run<Fwd128>(q, k, v, o, lse, BH, N, d, scale, causal, st);
-    case 192:
+    case 192: return run<Fwd192>(q, k, v, o, lse, BH, N, d, scale, causal, st);
     case 256: return run<Fwd256>(q, k, v, o, lse, BH, N, d, scale, causal, st);
   }
   return FA_ERR_UNSUPPORTED;
