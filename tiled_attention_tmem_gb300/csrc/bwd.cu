@@ -17,7 +17,7 @@ using KV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
 using KV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
 // d = 192: dV and dK for all 192 columns fit TMEM next to S and dP, so no d split.
 using KV7_192 = BwdKVCfg<192, 64, false, 1, 2, false>;
-using KV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true>;
+using KV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true, true>;
 // dQ kernel configurations <d, keys per tile, K/V ring slots>.
 using Q7_64 = BwdQCfg<64, 128, 6>;
 using Q7_128 = BwdQCfg<128, 128, 4>;

@@ -157,6 +157,10 @@ __global__ void __launch_bounds__(256) bwd_conv_kernel(const ConvParams p) {
 // VT: V lives in TMEM (written by the compute warps, thread = key row) and
 // dP^T = V dO^T takes A from TMEM; the 64 KB of shared memory this saves at
 // d = 256 holds a second query stage.
+// OS (7-GEMM, d = 256): the two work items of a key tile split the outputs
+// instead of the columns of d: item h = 0 computes S^T, P^T and dV only (no
+// dP^T), item h = 1 computes S^T, dP^T, dS^T and dK; each keeps one 256-column
+// accumulator in the same TMEM columns.
 struct BwdKVParams {
   CUtensorMap q_map;   // box {64, BM, 1}
   CUtensorMap k_map;   // box {64, 128, 1}
@@ -179,10 +183,10 @@ struct BwdKVParams {
   int* sched; // next unclaimed work item (zero at launch)
 };
 
-template <int D_, int BM_, bool DQ_, int DSPLIT_, int QS_, bool SEP_, bool VT_ = false>
+template <int D_, int BM_, bool DQ_, int DSPLIT_, int QS_, bool SEP_, bool VT_ = false, bool OS_ = false>
 struct BwdKVCfg {
   static constexpr int D = D_, BM = BM_, DSPLIT = DSPLIT_, QS = QS_;
-  static constexpr bool DQ = DQ_, SEP = SEP_, VT = VT_;
+  static constexpr bool DQ = DQ_, SEP = SEP_, VT = VT_, OS = OS_;
   // EARLY: the compute warps load all of S^T / dP^T into registers and release
   // those TMEM columns at once, so S^T(i+1), dP^T(i+1) run during the softmax of i.
   static constexpr bool EARLY = SEP && BM == 64;
@@ -194,7 +198,7 @@ struct BwdKVCfg {
   static constexpr int DRAIN_W0 = 4 + 4 * NCW;  // first dQ drain warp (5-GEMM)
   static constexpr bool DQ_T = DQ && D == 128;  // dQ^T (lanes = d) vs dQ (lanes = query)
   static constexpr int BN = 128;
-  static constexpr int DH = D / DSPLIT;
+  static constexpr int DH = OS ? D : D / DSPLIT;  // accumulator columns per item
   static constexpr int PANELS = D / 64;
   static constexpr uint32_t KV_PANEL = BN * 128;
   static constexpr uint32_t KV_TILE = PANELS * KV_PANEL;
@@ -229,7 +233,7 @@ struct BwdKVCfg {
   static constexpr int T_PT = SEP ? 2 * BM : T_ST;
   static constexpr int T_DST = SEP ? 2 * BM + BM / 2 : T_DPT;
   static constexpr int T_ACC = SEP ? 3 * BM : 2 * BM;
-  static constexpr int T_DV = T_ACC, T_DK = T_ACC + DH, T_DQ = T_ACC + 2 * DH;
+  static constexpr int T_DV = T_ACC, T_DK = T_ACC + (OS ? 0 : DH), T_DQ = T_ACC + (OS ? 1 : 2) * DH;
   static constexpr int DQ_COLS = DQ ? (DQ_T ? BM : D) : 0;
   static constexpr int T_V = T_DQ + DQ_COLS;  // VT: V as packed bf16 pairs, D / 2 columns
   static constexpr int TMEM_USED = T_V + (VT ? D / 2 : 0);
@@ -251,6 +255,7 @@ struct BwdKVCfg {
   static_assert(!DQ || D == 64 ? true : (D == 128 && BM == 64), "dQ^T path needs M = d = 128");
   static_assert(!(DQ && D == 64) || BM == 128, "dQ path needs M = BM = 128");
   static_assert(!VT || (!EARLY && NCW == 1), "V in TMEM is written by the single compute warpgroup");
+  static_assert(!OS || (VT && !DQ && !SEP && DSPLIT == 2), "output split: dV item and dK item per key tile");
 };
 
 template <class C>
@@ -483,16 +488,29 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           issue_dp(s);
         };
         auto issue_acc = [&](int s, int h, bool first) {
-          const uint32_t dob = stage_do(s) + h * (DH / 64) * C::QD_PANEL;
-          const uint32_t qb = stage_q(s) + h * (DH / 64) * C::QD_PANEL;
+          const int hoff = C::OS ? 0 : h;  // d part of the accumulators
+          const uint32_t dob = stage_do(s) + hoff * (DH / 64) * C::QD_PANEL;
+          const uint32_t qb = stage_q(s) + hoff * (DH / 64) * C::QD_PANEL;
+          if (!C::OS || h == 0) {
 #pragma unroll
-          for (int k = 0; k < BM / 16; ++k)
-            mma_ts(tmem + C::T_DV, tmem + C::T_PT + 8 * k, desc_mnmajor(dob, C::QD_PANEL, 16 * k), idAcc,
-                   (!first || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BM / 16; ++k)
+              mma_ts(tmem + C::T_DV, tmem + C::T_PT + 8 * k, desc_mnmajor(dob, C::QD_PANEL, 16 * k), idAcc,
+                     (!first || k > 0) ? 1u : 0u);
+          }
+          if (!C::OS || h == 1) {
 #pragma unroll
-          for (int k = 0; k < BM / 16; ++k)
-            mma_ts(tmem + C::T_DK, tmem + C::T_DST + 8 * k, desc_mnmajor(qb, C::QD_PANEL, 16 * k), idAcc,
-                   (!first || k > 0) ? 1u : 0u);
+            for (int k = 0; k < BM / 16; ++k)
+              mma_ts(tmem + C::T_DK, tmem + C::T_DST + 8 * k, desc_mnmajor(qb, C::QD_PANEL, 16 * k), idAcc,
+                     (!first || k > 0) ? 1u : 0u);
+          }
+        };
+        // OS: the dV item needs no dP^T.
+        auto issue_sdp_h = [&](int s, int h) {
+          issue_s(s);
+          if (C::OS && h == 0)
+            mma_commit(BAR(C::B_SDP));
+          else
+            issue_dp(s);
         };
         auto issue_dq = [&]() {
           const uint32_t ds = sbase + C::OFF_DS;
@@ -572,6 +590,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
             mma_commit(BAR(C::B_KVEMPTY));
           }
         } else {
+          int nv = 0;  // items whose V the compute warps wrote into TMEM (VT)
           for (int r = 0; ok; ++r) {
             const int w = item_warp(r);
             if (w < 0 || w >= p.items) break;
@@ -582,10 +601,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
               break;
             tc_fence_after();
             issue_s(g % QS);
-            // VT: the compute warps have written this item's V into TMEM.
-            if (C::VT && !wait_warp(BAR(C::B_VREADY), nkv & 1, ab, (kKBwdKV << 8) | 19)) break;
-            tc_fence_after();
-            issue_dp(g % QS);
+            if (C::OS && I.h == 0) {
+              mma_commit(BAR(C::B_SDP));
+            } else {
+              // VT: the compute warps have written this item's V into TMEM.
+              if (C::VT && !wait_warp(BAR(C::B_VREADY), nv & 1, ab, (kKBwdKV << 8) | 19)) break;
+              if (C::VT) ++nv;
+              tc_fence_after();
+              issue_dp(g % QS);
+            }
             for (int i = 0; i < I.n; ++i, ++g) {
               const int s = g % QS;
               const int s1 = (g + 1) % QS;
@@ -601,7 +625,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
                   break;
                 }
                 tc_fence_after();
-                issue_sdp(s1);
+                issue_sdp_h(s1, I.h);
               }
               if (!issue_tail(g, s, I.h, i == 0)) {
                 ok = false;
@@ -613,7 +637,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
                   break;
                 }
                 tc_fence_after();
-                issue_sdp(s1);
+                issue_sdp_h(s1, I.h);
               }
             }
             if (!ok) break;
@@ -646,16 +670,19 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         const bool key_ok = kj < p.N;
         if (I.n <= 0) {
           // No query can see this key tile: zero gradients.
+          const int c_off = C::OS ? 0 : I.h * DH;
           if (key_ok && cw == 0)
             for (int c = 0; c < DH; c += 8) {
-              if (I.h * DH + c < p.hd) {
-                *reinterpret_cast<uint4*>(p.dv + ((size_t)I.bh * p.N + kj) * p.hd + I.h * DH + c) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(p.dk + ((size_t)I.bh * p.N + kj) * p.hd + I.h * DH + c) = make_uint4(0, 0, 0, 0);
+              if (c_off + c < p.hd) {
+                if (!C::OS || I.h == 0)
+                  *reinterpret_cast<uint4*>(p.dv + ((size_t)I.bh * p.N + kj) * p.hd + c_off + c) = make_uint4(0, 0, 0, 0);
+                if (!C::OS || I.h == 1)
+                  *reinterpret_cast<uint4*>(p.dk + ((size_t)I.bh * p.N + kj) * p.hd + c_off + c) = make_uint4(0, 0, 0, 0);
               }
             }
           continue;
         }
-        if constexpr (C::VT) {
+        if (C::VT && (!C::OS || I.h == 1)) {
           // This item's V row kj as packed bf16 pairs into TMEM lane r: the A
           // operand of dP^T = V dO^T.  The previous item's dP^T MMAs, the last
           // readers of these columns, completed before its last S^T / dP^T
@@ -795,8 +822,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           if (C::NCW == 2 && which != cw) continue;  // two warpgroups: one stores dV, the other dK
-          uint16_t* dst = (which == 0 ? p.dv : p.dk) + (size_t)I.bh * p.N * p.hd + I.h * DH;
-          const int cols = min(DH, p.hd - I.h * DH);  // stored columns of this d part
+          if (C::OS && which != I.h) continue;       // output split: this item's one accumulator
+          const int c_off = C::OS ? 0 : I.h * DH;    // first column of this item's d part
+          uint16_t* dst = (which == 0 ? p.dv : p.dk) + (size_t)I.bh * p.N * p.hd + c_off;
+          const int cols = min(DH, p.hd - c_off);  // stored columns of this d part
           const float mul = which == 0 ? 1.f : p.scale;
           const uint32_t tacc = trow + (which == 0 ? C::T_DV : C::T_DK);
           if constexpr (C::DQ) {

@@ -158,7 +158,7 @@ using NKV5_128 = BwdKVCfg<128, 64, true, 1, 3, true>;
 using NKV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
 using NKV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
 using NKV7_192 = BwdKVCfg<192, 64, false, 1, 2, false>;
-using NKV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true>;
+using NKV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true, true>;
 using NQ7_64 = BwdQCfg<64, 128, 6>;
 using NQ7_128 = BwdQCfg<128, 128, 4>;
 using NQ7_192 = BwdQCfg<192, 64, 7, true>;
