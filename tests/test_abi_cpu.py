@@ -102,8 +102,9 @@ def test_workspace_sizes(lib):
         if b.lib().fa_bwd_launches(2, 3, 300, d, b.FA_BWD_5GEMM, 0) > 0:
             w5 = b.fa_bwd_workspace_size(2, 3, 300, d, b.FA_BWD_5GEMM)
             assert w5 >= 4 * 6 * 384 * (d + 1)
-    # head dims 96 and 192 run on zero-padded 128 / 256 tiles: the fp32 dQ
-    # accumulator has the padded width
+    # head dim 96 runs on zero-padded 128 tiles: the fp32 dQ accumulator has the
+    # padded width.  Head dim 192 has no 5-GEMM kernel (its dV, dK and dQ
+    # accumulators do not fit TMEM together).
     assert (b.fa_bwd_workspace_size(2, 3, 300, 96, b.FA_BWD_5GEMM)
             == b.fa_bwd_workspace_size(2, 3, 300, 128, b.FA_BWD_5GEMM))
     assert b.fa_bwd_workspace_size(2, 3, 300, 192, b.FA_BWD_5GEMM) == 0 or \
