@@ -26,7 +26,7 @@ SMALL = [
     (1, 2, 256, 256, True, 0.5, 0.0, 1.0 / 16),
     (1, 1, 130, 256, False, 1.0, 0.0, None),
     (1, 1, 640, 256, False, 1.0, 3.0, None),
-    # head dims 96 and 192 (zero-padded 128 / 256 tiles)
+    # head dims 96 (zero-padded 128 tiles) and 192 (its own 192-column tiles)
     (1, 2, 300, 96, True, 1.0, 0.0, None),
     (2, 1, 256, 96, False, 1.0, 3.0, None),
     (1, 2, 200, 192, True, 1.0, 0.0, None),

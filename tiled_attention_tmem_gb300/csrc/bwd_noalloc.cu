@@ -175,7 +175,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   if (B < 0 || H < 0 || N < 0) return FA_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f) || (causal != 0 && causal != 1)) return FA_ERR_INVALID_ARG;
   if (variant != FA_BWD_AUTO && variant != FA_BWD_5GEMM && variant != FA_BWD_7GEMM) return FA_ERR_INVALID_ARG;
-  const int D = padded_head_dim(d);  // 96 and 192 run on zero-padded 128 / 256 tiles
+  const int D = padded_head_dim(d);  // 96 runs on zero-padded 128 tiles; 192 on its own (see below)
   if (D == 0) return FA_ERR_UNSUPPORTED;
   if ((long long)B * H > 0x7fffffffLL || (long long)N > 0x7fffffffLL / 2) return FA_ERR_INVALID_ARG;
   if ((long long)B * H * N == 0) return FA_OK;

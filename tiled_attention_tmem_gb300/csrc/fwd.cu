@@ -10,10 +10,11 @@ namespace {
 // Per head dimension: query tiles per CTA, keys per tile, K/V ring depth.
 //  d = 64 : 2 x 128 query rows, 128 keys, 6 stages (Q 32 KiB + ring 96 KiB)
 //  d = 128: 2 x 128 query rows, 128 keys, 4 stages (Q 64 KiB + ring 128 KiB)
-//  d = 256: 1 x 128 query rows, 128 keys, 2 stages (Q 64 KiB + ring 128 KiB)
-// d = 96 and d = 192 run the d = 128 and d = 256 kernels: the TMA boxes read
-// columns past d as zeros, which leave S = QK^T unchanged and give zero
-// output columns that are not stored.
+//  d = 192: 1 x 128 query rows, 64 keys, 8 stages, Q in TMEM (ring 192 KiB)
+//  d = 256: 1 x 128 query rows, 64 keys, 6 stages, Q in TMEM (ring 192 KiB)
+// d = 96 runs the d = 128 kernel: the TMA boxes read columns past d as zeros,
+// which leave S = QK^T unchanged and give zero output columns that are not
+// stored.
 using Fwd64 = FwdCfg<64, 2, 128, 6>;
 using Fwd128 = FwdCfg<128, 2, 128, 4>;
 using Fwd192 = FwdCfg<192, 1, 64, 8, true>;

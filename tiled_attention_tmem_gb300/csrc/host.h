@@ -73,8 +73,10 @@ fa_status run_fwd(const void* q, const void* k, const void* v, void* o, float* l
                   int d, float scale, int causal, cudaStream_t st);
 int fwd_launch_count(int d);
 
-// Head dims the kernels support and the kernel head dim (64, 128 or 256) that
-// serves each: 96 and 192 run on zero-padded 128 / 256 tiles.  0 if unsupported.
+// Head dims the kernels support and the head dim (64, 128 or 256) whose
+// workspace layout, preprocess and variant rules serve each: 96 runs the 128
+// kernels on zero-padded tiles; 192 has its own forward, dK/dV and dQ kernels
+// but the 256 preprocess and rules (no 5-GEMM).  0 if unsupported.
 inline int padded_head_dim(int d) {
   return d == 64 ? 64 : (d == 96 || d == 128) ? 128 : (d == 192 || d == 256) ? 256 : 0;
 }
