@@ -42,9 +42,14 @@ def check_fwd(o, lse, o_ref, lse_ref, what=""):
 
 
 def check_grads(got, ref, what=""):
+    # A tensor whose reference is identically zero (N = 1 gives dQ = dK = 0 exactly)
+    # would be held to exactly zero by the relative bound; fp32 rounding of dP - D
+    # leaves ~1e-6 there, so it is held to the largest gradient reference instead.
+    scales = [float(np.max(np.abs(r))) if r.size else 0.0 for r in ref]
+    floor = max(scales)
     out = []
-    for name, g, r in zip(("dQ", "dK", "dV"), got, ref):
-        scale = float(np.max(np.abs(r))) if r.size else 0.0
+    for name, g, r, s in zip(("dQ", "dK", "dV"), got, ref, scales):
+        scale = s if s > 0 else floor
         e = max_abs(g, r)
         assert e <= TOL_GRAD_REL * scale, f"{what} {name} max abs err {e:.3e} > {TOL_GRAD_REL}*{scale:.3e}"
         out.append(e / scale if scale else 0.0)

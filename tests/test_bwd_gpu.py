@@ -30,6 +30,9 @@ SMALL = [
     (2, 1, 256, 96, False, 1.0, 3.0, None),
     (1, 2, 200, 192, True, 1.0, 0.0, None),
     (1, 1, 384, 192, False, 0.5, 0.0, None),
+    (1, 2, 17, 192, True, 1.0, 0.0, None),
+    (1, 1, 1, 256, False, 1.0, 0.0, None),
+    (2, 1, 65, 256, True, 0.5, 0.0, 1.0 / 16),
     # more work items than SMs: each persistent CTA claims several, short ones among them
     (2, 96, 256, 256, True, 0.5, 0.0, 1.0 / 16),
     (1, 200, 256, 128, True, 1.0, 0.0, None),

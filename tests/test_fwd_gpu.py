@@ -31,6 +31,10 @@ SMALL = [
     (2, 1, 256, 96, False, 1.0, 3.0, None),
     (1, 2, 200, 192, True, 1.0, 0.0, None),
     (1, 1, 384, 192, False, 0.5, 0.0, None),
+    # one key step, and a single row, at the head dims with Q in TMEM
+    (1, 2, 17, 192, True, 1.0, 0.0, None),
+    (1, 1, 1, 256, False, 1.0, 0.0, None),
+    (2, 1, 65, 256, True, 0.5, 0.0, 1.0 / 16),
     # more work items than SMs, so that each persistent CTA runs several items,
     # short ones (one or two key tiles) among them
     (2, 96, 256, 256, True, 0.5, 0.0, 1.0 / 16),
