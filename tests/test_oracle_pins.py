@@ -259,6 +259,48 @@ def test_affine_values():
         np.testing.assert_allclose(o2, -2.5 * o + bvec, rtol=1e-12, atol=1e-12)
 
 
+def test_permutation_equivariance():
+    """Without a mask, permuting keys and values together changes nothing but the
+    order of dK and dV; permuting queries (with dO) permutes O, LSE and dQ alike."""
+    n, d = 19, 7
+    q, k, v, do = (rand(1, 1, n, d) for _ in range(4))
+    perm = np.random.default_rng(7).permutation(n)
+    o, lse = A.forward(q, k, v, 0.4, False)
+    dq, dk, dv = A.backward(q, k, v, do, 0.4, False)
+    o2, lse2 = A.forward(q, k[:, :, perm], v[:, :, perm], 0.4, False)
+    dq2, dk2, dv2 = A.backward(q, k[:, :, perm], v[:, :, perm], do, 0.4, False)
+    np.testing.assert_allclose(o2, o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(dq2, dq, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dk2, dk[:, :, perm], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dv2, dv[:, :, perm], rtol=1e-11, atol=1e-12)
+    o3, lse3 = A.forward(q[:, :, perm], k, v, 0.4, False)
+    dq3, dk3, dv3 = A.backward(q[:, :, perm], k, v, do[:, :, perm], 0.4, False)
+    np.testing.assert_allclose(o3, o[:, :, perm], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse3, lse[:, :, perm], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(dq3, dq[:, :, perm], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dk3, dk, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(dv3, dv, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_scale_reparametrisation(causal):
+    """Only the product scale * Q enters the scores: Q -> c Q with scale -> scale / c
+    leaves O, LSE, dK and dV unchanged and divides dQ by c."""
+    n, d = 15, 5
+    q, k, v, do = (rand(1, 2, n, d) for _ in range(4))
+    c = 3.7
+    o, lse = A.forward(q, k, v, 0.6, causal)
+    o2, lse2 = A.forward(c * q, k, v, 0.6 / c, causal)
+    np.testing.assert_allclose(o2, o, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse2, lse, rtol=1e-12, atol=1e-13)
+    dq, dk, dv = A.backward(q, k, v, do, 0.6, causal)
+    dq2, dk2, dv2 = A.backward(c * q, k, v, do, 0.6 / c, causal)
+    np.testing.assert_allclose(dq2, dq / c, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dk2, dk, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dv2, dv, rtol=1e-10, atol=1e-12)
+
+
 def test_forward_rows_matches_forward():
     q, k, v = rand(1, 2, 40, 8), rand(1, 2, 40, 8), rand(1, 2, 40, 8)
     for causal in (False, True):
@@ -350,19 +392,30 @@ def _mutant_backward(kind):
                 dp = do[b, h] @ v[b, h].T
                 ds = p * (dp - dd[:, None]) if kind != "sign" else p * (dd[:, None] - dp)
                 dv = p.T @ do[b, h] if kind != "transpose" else p @ do[b, h]
-                dq = scale * ds @ k[b, h]
+                dq = (scale if kind != "dqnoscale" else 1.0) * ds @ k[b, h]
                 dk = (scale if kind != "noscale" else 1.0) * ds.T @ q[b, h]
                 out[0][b, h], out[1][b, h], out[2][b, h] = dq, dk, dv
         return tuple(out)
     return bwd
 
 
-@pytest.mark.parametrize("kind", ["sign", "transpose", "noscale"])
+@pytest.mark.parametrize("kind", ["sign", "transpose", "noscale", "dqnoscale"])
 def test_planted_mistakes_are_caught(kind):
     rng = np.random.default_rng(99)
     q, k, v, do = (rand(1, 1, 5, 3, rng=rng) for _ in range(4))
     errs = _fd_errors(q, k, v, do, 0.37, False, backward=_mutant_backward(kind))
     assert max(errs) > 1e-3, f"planted mistake '{kind}' slipped through: {errs}"
+
+
+def test_reparametrisation_pin_catches_a_missing_dq_scale():
+    """The scale reparametrisation pin, applied to a backward that forgets the scale
+    on dQ only, fails (dQ would not scale by 1 / c)."""
+    q, k, v, do = (rand(1, 1, 9, 4) for _ in range(4))
+    bwd = _mutant_backward("dqnoscale")
+    c = 3.7
+    dq = bwd(q, k, v, do, 0.6, False)[0]
+    dq2 = bwd(c * q, k, v, do, 0.6 / c, False)[0]
+    assert not np.allclose(dq2, dq / c, rtol=1e-6, atol=1e-9)
 
 
 def test_planted_causal_off_by_one_is_caught():
