@@ -193,8 +193,13 @@ struct BwdKVCfg {
   // Compute warpgroups: the 5-GEMM EARLY kernel splits the BM query columns
   // (and the dV / dK epilogue) over two warpgroups to halve the per-tile
   // critical path; the 7-GEMM kernel measured faster with one.
-  static constexpr int NCW = (EARLY && DQ) ? 2 : 1;
+  static constexpr int NCW = (DQ && (EARLY || D == 64)) ? 2 : 1;
   static constexpr int CW = BM / NCW;
+  // Without separate P^T / dS^T columns, each compute warpgroup packs its results
+  // over the first half of its own S^T / dP^T columns (no warpgroup overwrites
+  // columns the other still reads).  Packed column of query column c:
+  static constexpr bool SPLITPACK = !SEP && NCW == 2;
+  static __device__ __forceinline__ int pcol(int c) { return SPLITPACK ? (c / CW) * CW + (c % CW) / 2 : c / 2; }
   static constexpr int DRAIN_W0 = 4 + 4 * NCW;  // first dQ drain warp (5-GEMM)
   static constexpr bool DQ_T = DQ && D == 128;  // dQ^T (lanes = d) vs dQ (lanes = query)
   static constexpr int BN = 128;
@@ -494,13 +499,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           if (!C::OS || h == 0) {
 #pragma unroll
             for (int k = 0; k < BM / 16; ++k)
-              mma_ts(tmem + C::T_DV, tmem + C::T_PT + 8 * k, desc_mnmajor(dob, C::QD_PANEL, 16 * k), idAcc,
+              mma_ts(tmem + C::T_DV, tmem + C::T_PT + C::pcol(16 * k), desc_mnmajor(dob, C::QD_PANEL, 16 * k), idAcc,
                      (!first || k > 0) ? 1u : 0u);
           }
           if (!C::OS || h == 1) {
 #pragma unroll
             for (int k = 0; k < BM / 16; ++k)
-              mma_ts(tmem + C::T_DK, tmem + C::T_DST + 8 * k, desc_mnmajor(qb, C::QD_PANEL, 16 * k), idAcc,
+              mma_ts(tmem + C::T_DK, tmem + C::T_DST + C::pcol(16 * k), desc_mnmajor(qb, C::QD_PANEL, 16 * k), idAcc,
                      (!first || k > 0) ? 1u : 0u);
           }
         };
@@ -723,8 +728,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           // for the 5-GEMM variant, dS^T row r into the [128 keys][BM queries]
           // swizzled shared-memory tile read by the dQ MMA.
           auto store_chunk = [&](int c0, const uint32_t* pp, const uint32_t* pd) {
-            tmem_st_32x32b_x16(trow + C::T_PT + (c0 >> 1), pp);
-            tmem_st_32x32b_x16(trow + C::T_DST + (c0 >> 1), pd);
+            tmem_st_32x32b_x16(trow + C::T_PT + C::pcol(c0), pp);
+            tmem_st_32x32b_x16(trow + C::T_DST + C::pcol(c0), pd);
             if constexpr (C::DQ) {
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
@@ -786,14 +791,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
             for (int c0 = 0; c0 < C::CW; c0 += 32) compute_chunk(c_lo + c0, sr + c0, dr + c0, c0 >> 1);
           } else {
 #pragma unroll
-            for (int c0 = 0; c0 < BM; c0 += 32) {
+            for (int c0 = c_lo; c0 < c_lo + C::CW; c0 += 32) {
               uint32_t sr[32], dr[32];
               tmem_ld_32x32b_x32(trow + C::T_ST + c0, sr);
               tmem_ld_32x32b_x32(trow + C::T_DPT + c0, dr);
               tmem_wait_ld();
               reg_fence<32>(sr);
               reg_fence<32>(dr);
-              compute_chunk(c0, sr, dr, C::SEP ? (c0 >> 1) : 0);
+              compute_chunk(c0, sr, dr, C::SEP ? ((c0 - c_lo) >> 1) : 0);
               if constexpr (!C::SEP) store_chunk(c0, pk_p, pk_ds);
             }
           }
