@@ -39,11 +39,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum).  Keyed by the workload and the
 # hash of the kernel sources it was taken on; any source change voids it.
 NCU_TRAFFIC = {
-    ("b4_h16_n2048_d128_causal", "bwd_kv5", "2829ed4449f1bcf8"): 311.4e6,
-    ("b4_h16_n2048_d128_causal", "fwd", "2829ed4449f1bcf8"): 152.8e6,
-    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_kv7", "2829ed4449f1bcf8"): 175.8e6,
-    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_q7", "2829ed4449f1bcf8"): 196.2e6,
-    ("b2_h8_n4096_d256_causal_sigma0.5", "fwd", "2829ed4449f1bcf8"): 158.3e6,
+    ("b4_h16_n2048_d128_causal", "bwd_kv5", "a5103063fe84cb75"): 311.5e6,
+    ("b4_h16_n2048_d128_causal", "fwd", "a5103063fe84cb75"): 152.2e6,
+    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_kv7", "a5103063fe84cb75"): 175.4e6,
+    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_q7", "a5103063fe84cb75"): 195.0e6,
+    ("b2_h8_n4096_d256_causal_sigma0.5", "fwd", "a5103063fe84cb75"): 157.5e6,
 }
 
 
