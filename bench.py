@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--variant", choices=["auto", "5", "7"], default="auto")
+    ap.add_argument("--splits", default="auto",
+                    help="forward key parts per query block: 'auto' (the library's cost model) or a count")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     return ap.parse_args()
@@ -243,12 +245,16 @@ def run_ours(args, rank, world, local_rank):
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     ws = torch.empty(b.fa_bwd_workspace_size(w.B, w.H, w.N, w.d, chosen), dtype=torch.uint8, device=dev)
+    splits = (b.fa_fwd_choose_splits(w.B, w.H, w.N, w.d, w.causal) if args.splits == "auto"
+              else int(args.splits))
+    split_ws = torch.empty(max(1, b.fa_fwd_splitkv_workspace_size(w.B, w.H, w.N, w.d, splits)),
+                           dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)  # > 129 MB L2
     scale = w.softmax_scale
     stream = torch.cuda.current_stream()
 
     def step():
-        api.attention_forward(q, k, v, scale, w.causal, out=o, lse=lse)
+        api.attention_forward(q, k, v, scale, w.causal, out=o, lse=lse, splits=splits, workspace=split_ws)
         api.attention_backward(q, k, v, o, do, lse, scale, w.causal, variant=chosen, workspace=ws,
                                grads=grads)
 
@@ -298,7 +304,7 @@ def run_ours(args, rank, world, local_rank):
     api.check_device_error()
     flops_step = w.fwd_flops + w.bwd_flops
     value, total_s = aggregate_throughput(sum(times_ms) / 1e3, flops_step, args.steps, dev)
-    launches = args.steps * (b.fa_fwd_launches(w.B, w.H, w.N, w.d)
+    launches = args.steps * (b.fa_fwd_splitkv_launches(w.B, w.H, w.N, w.d, splits)
                              + b.fa_bwd_launches(w.B, w.H, w.N, w.d, chosen, w.causal))
     assert sum(n for n, _ in prof.values()) == launches, "launch count mismatch"
 
@@ -327,7 +333,8 @@ def run_ours(args, rank, world, local_rank):
                 "frac": ach / peak, "traffic": tr, "traffic_unit": "bytes per launch (ncu dram read + write)",
                 "peak_source": f"bf16_tflops (burst) of {peak_src} peaks",
                 "frac_of_sustained": ach / float(peaks["bf16_tflops_sustained"])}
-    fwd_tf = w.fwd_flops / (kernels["fwd"]["ms_avg"] / 1e3) / 1e12 if "fwd" in kernels else None
+    fwd_ms = sum(kernels[n_]["ms_avg"] for n_ in ("fwd", "fwd_merge") if n_ in kernels)
+    fwd_tf = w.fwd_flops / (fwd_ms / 1e3) / 1e12 if fwd_ms else None
     bwd_ms = sum(kernels[n_]["ms_avg"] for n_ in ("bwd_pre", "bwd_kv5", "bwd_conv", "bwd_kv7", "bwd_q7")
                  if n_ in kernels)
     bwd_tf = w.bwd_flops / (bwd_ms / 1e3) / 1e12 if bwd_ms else None
@@ -357,6 +364,8 @@ def run_ours(args, rank, world, local_rank):
         + (4 * bh * npad * dk_ if chosen == b.FA_BWD_5GEMM else 0),
         # fp32 dQ accumulator read, bf16 dQ written
         "bwd_conv": 4 * bh * w.N * dk_ + 2 * bh * w.N * w.d,
+        # split-KV merge: fp32 parts and their log-sum-exps read, bf16 O and LSE written
+        "fwd_merge": 4 * splits * bh * w.N * (w.d + 1) + 2 * bh * w.N * w.d + 4 * bh * w.N,
     }
     hbm = {}
     for name_, bytes_ in hbm_bytes.items():
@@ -402,7 +411,8 @@ def run_ours(args, rank, world, local_rank):
                     s_cmp.wait_event(ev_out[bi][c])  # step i-2's outputs have been copied out
             qq, kk, vv, dd_ = dev_in[bi]
             oo, ll, gq, gk, gv = dev_out[bi]
-            api.attention_forward(qq, kk, vv, scale, w.causal, out=oo, lse=ll, stream=s_cmp.cuda_stream)
+            api.attention_forward(qq, kk, vv, scale, w.causal, out=oo, lse=ll, stream=s_cmp.cuda_stream,
+                                  splits=splits, workspace=split_ws)
             api.attention_backward(qq, kk, vv, oo, dd_, ll, scale, w.causal, variant=chosen, workspace=ws,
                                    grads=(gq, gk, gv), stream=s_cmp.cuda_stream)
             ev_cmp[bi].record(s_cmp)
@@ -445,6 +455,7 @@ def run_ours(args, rank, world, local_rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                        "scale": scale, "bwd_variant": f"{chosen}-GEMM" + (" (auto)" if variant == 0 else ""),
+                       "fwd_splits": splits,
                        "l2": "flushed (256 MiB write) between timed steps, outside the timed events",
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,

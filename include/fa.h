@@ -75,6 +75,38 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int B, int H, int N, int d, float scale, int causal, void* stream);
 
 /*
+ * Split-KV forward: the same results as fa_fwd (up to fp32 rounding of the
+ * merge), for shapes with too few query blocks (B*H*ceil(N/rows) below the SM
+ * count) to fill the GPU.  Each query block's key tiles are cut into `splits`
+ * contiguous parts of equal tile count; each part is a separate work item that
+ * writes its normalised fp32 partial output O_s = (sum_j p_ij V_j) / l_s and its
+ * log2-domain log-sum-exp L_s, and a second kernel merges the parts exactly:
+ *   L = log2 sum_s 2^(L_s),  O = sum_s 2^(L_s - L) O_s,  LSE = L ln 2,
+ * the block merge of the running (max, sum) statistics in "ELI5: FlashAttention"
+ * (softmax statistics passage) applied to whole parts.  A part with no key
+ * visible to a row has L_s = -inf and weight 0.
+ * splits: 1..FA_FWD_MAX_SPLITS (1 is fa_fwd, with no workspace and one launch).
+ * workspace: device memory of at least fa_fwd_splitkv_workspace_size bytes,
+ * 256-byte aligned, owned by the caller and not shared with a concurrent call:
+ *   fp32 parts [splits, B, H, N, d] at offset 0, then (256-byte aligned) fp32
+ *   log2-domain LSEs [splits, B, H, N].
+ * Errors as fa_fwd, plus FA_ERR_INVALID_ARG for splits out of range and
+ * FA_ERR_WORKSPACE for a missing, misaligned or short workspace.
+ */
+#define FA_FWD_MAX_SPLITS 64
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int splits);
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, float scale, int causal, int splits,
+                         void* workspace, size_t workspace_bytes, void* stream);
+/*
+ * Parts per query block for fa_fwd_splitkv that the library's cost model
+ * predicts fastest on the current device (1 = plain fa_fwd); 1 for invalid
+ * shapes.  The model weighs the rounds of work items over the SMs against the
+ * merge kernel's fp32 traffic.
+ */
+int fa_fwd_choose_splits(int B, int H, int N, int d, int causal);
+
+/*
  * Bytes of device workspace fa_bwd needs for this shape and variant
  * (FA_BWD_AUTO: the largest over the variants).  0 for invalid shapes.
  *   log2-domain LSE per row:           4*B*H*Npad bytes
@@ -174,7 +206,8 @@ enum {
   FA_KERNEL_BWD_CONV = 3, /* 5-GEMM dQ fp32 -> bf16 */
   FA_KERNEL_BWD_KV7 = 4,  /* 7-GEMM dK/dV kernel */
   FA_KERNEL_BWD_Q7 = 5,   /* 7-GEMM dQ kernel */
-  FA_KERNEL_KINDS = 6
+  FA_KERNEL_FWD_MERGE = 6, /* split-KV merge of the forward's parts */
+  FA_KERNEL_KINDS = 7
 };
 typedef struct {
   int launches[FA_KERNEL_KINDS];
@@ -184,8 +217,9 @@ int fa_profile_start(void);
 int fa_profile_stop(fa_profile* out);
 const char* fa_kernel_name(int kind);
 
-/* Number of kernels one fa_fwd / fa_bwd call launches for this shape/variant. */
+/* Number of kernels one fa_fwd / fa_fwd_splitkv / fa_bwd call launches for this shape. */
 int fa_fwd_launches(int B, int H, int N, int d);
+int fa_fwd_splitkv_launches(int B, int H, int N, int d, int splits);
 int fa_bwd_launches(int B, int H, int N, int d, int variant, int causal);
 
 #ifdef __cplusplus

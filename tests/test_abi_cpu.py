@@ -114,6 +114,61 @@ def test_workspace_sizes(lib):
     assert b.fa_bwd_workspace_size(1, 1, 128, 64, 9) == 0
 
 
+def test_splitkv_validation(lib):
+    """Argument checks of the split-KV forward (none of these launch anything)."""
+    def call(B=1, H=2, N=128, d=64, scale=0.125, causal=0, splits=2, ws=A, wsb=1 << 30, q=A, lse=A):
+        return b.fa_fwd_splitkv(q, A, A, A, lse, B, H, N, d, scale, causal, splits, ws, wsb, None)
+
+    assert call(d=80) == b.FA_ERR_UNSUPPORTED
+    assert call(splits=0) == b.FA_ERR_INVALID_ARG
+    assert call(splits=-3) == b.FA_ERR_INVALID_ARG
+    assert call(splits=b.FA_FWD_MAX_SPLITS + 1) == b.FA_ERR_INVALID_ARG
+    assert call(scale=float("nan")) == b.FA_ERR_INVALID_ARG
+    assert call(q=0) == b.FA_ERR_INVALID_ARG
+    assert call(lse=A + 4) == b.FA_ERR_MISALIGNED
+    assert call(ws=0) == b.FA_ERR_WORKSPACE
+    assert call(ws=A + 16) == b.FA_ERR_WORKSPACE  # 16- but not 256-byte aligned
+    need = b.fa_fwd_splitkv_workspace_size(1, 2, 128, 64, 2)
+    assert call(wsb=need - 1) == b.FA_ERR_WORKSPACE
+    assert call(q=0, lse=0, ws=0, N=0) == b.FA_OK
+
+
+def test_splitkv_workspace_and_launches(lib):
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for d in (64, 96, 128, 192, 256):
+        for s in (2, 3, 16, b.FA_FWD_MAX_SPLITS):
+            got = b.fa_fwd_splitkv_workspace_size(2, 3, 300, d, s)
+            assert got == r256(4 * s * 6 * 300 * d) + r256(4 * s * 6 * 300), (d, s)
+        assert b.fa_fwd_splitkv_workspace_size(2, 3, 300, d, 1) == 0
+        assert b.fa_fwd_splitkv_launches(2, 3, 300, d, 1) == 1
+        assert b.fa_fwd_splitkv_launches(2, 3, 300, d, 5) == 2
+    assert b.fa_fwd_splitkv_workspace_size(2, 3, 300, 64, 0) == 0
+    assert b.fa_fwd_splitkv_workspace_size(2, 3, 300, 64, b.FA_FWD_MAX_SPLITS + 1) == 0
+    assert b.fa_fwd_splitkv_workspace_size(2, 3, 300, 100, 2) == 0
+    assert b.fa_fwd_splitkv_launches(2, 3, 0, 64, 2) == 0
+    assert b.fa_fwd_splitkv_launches(2, 3, 300, 64, 0) == 0
+
+
+def test_split_choice(lib):
+    """The split-KV cost model: no split once the query blocks fill the SMs, a split
+    for one long head (8192 rows: 32 or 64 query blocks), never more than 16 parts,
+    at least two key tiles per part, 1 for invalid shapes."""
+    assert b.fa_fwd_choose_splits(4, 16, 2048, 128, 1) == 1
+    assert b.fa_fwd_choose_splits(16, 16, 512, 64, 0) == 1
+    for d in (64, 96, 128, 192, 256):
+        for causal in (0, 1):
+            s = b.fa_fwd_choose_splits(1, 1, 8192, d, causal)
+            assert 2 <= s <= 16, (d, causal, s)
+            for N in (1, 100, 1000, 5000, 70000):
+                s = b.fa_fwd_choose_splits(1, 2, N, d, causal)
+                assert 1 <= s <= 16
+                tiles = -(-N // (128 if d <= 128 else 64))
+                assert s == 1 or tiles // s >= 2
+    assert b.fa_fwd_choose_splits(1, 1, 128, 100, 0) == 1
+    assert b.fa_fwd_choose_splits(1, 1, 0, 128, 0) == 1
+
+
 def test_strerror(lib):
     for s in range(7):
         assert b.fa_strerror(s)

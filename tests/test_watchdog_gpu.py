@@ -49,6 +49,8 @@ def test_kernels_skip_work_while_the_error_word_is_set():
     lse = torch.full((1, 1, 128), 7.0, dtype=torch.float32, device=q.device)
     assert b.fa_watchdog_selftest(stream) == b.FA_OK
     api.attention_forward(q, k, v, 0.125, False, out=o, lse=lse)
+    # the split-KV forward's part and merge kernels skip as well
+    api.attention_forward(q, k, v, 0.125, False, out=o, lse=lse, splits=2)
     status, _ = b.fa_get_device_error(stream)
     assert status == b.FA_ERR_DEVICE_TIMEOUT
     assert bool((o == 7.0).all()) and bool((lse == 7.0).all())

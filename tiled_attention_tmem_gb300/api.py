@@ -25,8 +25,13 @@ def _stream(stream):
 
 
 def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
-                      out=None, lse=None, stream=None):
-    """Returns (O bf16 [B,H,N,d], LSE fp32 [B,H,N])."""
+                      out=None, lse=None, stream=None, splits: int | None = 1, workspace=None):
+    """Returns (O bf16 [B,H,N,d], LSE fp32 [B,H,N]).
+
+    ``splits`` > 1 runs the split-KV form (``fa_fwd_splitkv``) with that many key
+    parts per query block; ``None`` takes ``fa_fwd_choose_splits``.  ``workspace``
+    (a uint8 CUDA tensor of ``splitkv_workspace_bytes`` or more) is allocated when
+    needed and not given."""
     import torch
     for t, n in ((q, "q"), (k, "k"), (v, "v")):
         _check(t, n, torch.bfloat16)
@@ -36,11 +41,27 @@ def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     o = torch.empty_like(q) if out is None else _check(out, "out", torch.bfloat16)
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    st = _b.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
-                   B, H, N, d, scale, int(causal), _stream(stream))
+    if splits is None:
+        splits = _b.fa_fwd_choose_splits(B, H, N, d, int(causal))
+    if splits == 1:
+        st = _b.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                       B, H, N, d, scale, int(causal), _stream(stream))
+        if st != _b.FA_OK:
+            raise _b.FaError(st, "fa_fwd")
+        return o, l
+    if workspace is None:
+        need = _b.fa_fwd_splitkv_workspace_size(B, H, N, d, splits)
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = _b.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
+                           B, H, N, d, scale, int(causal), splits, workspace.data_ptr(),
+                           workspace.numel(), _stream(stream))
     if st != _b.FA_OK:
-        raise _b.FaError(st, "fa_fwd")
+        raise _b.FaError(st, "fa_fwd_splitkv")
     return o, l
+
+
+def splitkv_workspace_bytes(B, H, N, d, splits) -> int:
+    return _b.fa_fwd_splitkv_workspace_size(B, H, N, d, splits)
 
 
 def workspace_bytes(B, H, N, d, variant=_b.FA_BWD_AUTO) -> int:

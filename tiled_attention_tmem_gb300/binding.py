@@ -22,6 +22,8 @@ FA_ERR_WORKSPACE = 4
 FA_ERR_LAUNCH = 5
 FA_ERR_DEVICE_TIMEOUT = 6
 
+FA_FWD_MAX_SPLITS = 64
+
 FA_BWD_AUTO = 0
 FA_BWD_5GEMM = 5
 FA_BWD_7GEMM = 7
@@ -33,6 +35,9 @@ _F = ctypes.c_float
 _SZ = ctypes.c_size_t
 SIGNATURES = {
     "fa_fwd": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _I, _VP]),
+    "fa_fwd_splitkv_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
+    "fa_fwd_splitkv": (_I, [_VP, _VP, _VP, _VP, _VP, _I, _I, _I, _I, _F, _I, _I, _VP, _SZ, _VP]),
+    "fa_fwd_choose_splits": (_I, [_I, _I, _I, _I, _I]),
     "fa_bwd_workspace_size": (_SZ, [_I, _I, _I, _I, _I]),
     "fa_bwd": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                     _I, _I, _I, _I, _F, _I, _I, _VP, _SZ, _VP]),
@@ -47,6 +52,7 @@ SIGNATURES = {
     "fa_profile_stop": (_I, [_VP]),
     "fa_kernel_name": (ctypes.c_char_p, [_I]),
     "fa_fwd_launches": (_I, [_I, _I, _I, _I]),
+    "fa_fwd_splitkv_launches": (_I, [_I, _I, _I, _I, _I]),
     "fa_bwd_launches": (_I, [_I, _I, _I, _I, _I, _I]),
 }
 
@@ -85,6 +91,20 @@ def fa_strerror(status: int) -> str:
 
 def fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, stream) -> int:
     return lib().fa_fwd(q, k, v, o, lse, B, H, N, d, float(scale), int(causal), stream)
+
+
+def fa_fwd_splitkv_workspace_size(B, H, N, d, splits) -> int:
+    return lib().fa_fwd_splitkv_workspace_size(B, H, N, d, splits)
+
+
+def fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, scale, causal, splits, workspace, workspace_bytes,
+                   stream) -> int:
+    return lib().fa_fwd_splitkv(q, k, v, o, lse, B, H, N, d, float(scale), int(causal), int(splits),
+                                workspace, workspace_bytes, stream)
+
+
+def fa_fwd_choose_splits(B, H, N, d, causal) -> int:
+    return lib().fa_fwd_choose_splits(B, H, N, d, int(causal))
 
 
 def fa_bwd_workspace_size(B, H, N, d, variant) -> int:
@@ -128,11 +148,15 @@ def fa_fwd_launches(B, H, N, d) -> int:
     return lib().fa_fwd_launches(B, H, N, d)
 
 
+def fa_fwd_splitkv_launches(B, H, N, d, splits) -> int:
+    return lib().fa_fwd_splitkv_launches(B, H, N, d, splits)
+
+
 def fa_bwd_launches(B, H, N, d, variant, causal=0) -> int:
     return lib().fa_bwd_launches(B, H, N, d, variant, int(causal))
 
 
-FA_KERNEL_KINDS = 6
+FA_KERNEL_KINDS = 7
 
 
 class FaProfile(ctypes.Structure):

@@ -29,6 +29,12 @@
 // double-buffered in TMEM and the order S_t(0) S_t(1) PV_t(0) S_t(2) PV_t(1) ...
 // lets the softmax warps run from one key tile to the next without waiting for
 // S.  K/V tiles are loaded in that order (K one step ahead of V).
+//
+// Split-KV (splits > 1): every query block becomes `splits` work items, item s
+// covering part s of the block's key tiles.  An item ends with O_s = O / l
+// normalised by its own sum (fp32) and its log2-domain log-sum-exp L_s = m + log2 l
+// (-inf where no key of the part is visible to the row); fwd_merge_kernel then
+// combines the parts with the same max/sum algebra as the online softmax.
 #pragma once
 #include <cuda_bf16.h>
 
@@ -50,7 +56,23 @@ struct FwdParams {
   float scale_log2;  // scale * log2(e)
   int causal;
   int group;  // heads per launch-order group
-  int items;  // work items (query blocks x heads); the grid is persistent over them
+  int items;  // work items (query blocks x heads x splits); the grid is persistent over them
+  int splits;    // key-range parts per query block (1: O and LSE are written directly)
+  float* opart;  // splits > 1: fp32 [splits, B*H, N, d], part s of row i = O_s(i) / l_s(i)
+  float* lpart;  // splits > 1: fp32 [splits, B*H, N], log2-domain L_s(i) (-inf: no visible key)
+};
+
+// Merge of split-KV parts: for each row, L = log2 sum_s 2^(L_s) and
+// O = sum_s 2^(L_s - L) O_s (bf16), LSE = L ln 2 (natural log, fp32).
+struct FwdMergeParams {
+  const float* opart;
+  const float* lpart;
+  uint16_t* o;
+  float* lse;
+  int* err;
+  long long rows;  // B*H*N
+  int dv;          // head dim (a multiple of 8)
+  int splits;
 };
 
 template <int D_, int NQ_, int BN_, int STAGES_, bool QT_ = false>
@@ -108,7 +130,9 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-template <class C>
+// SPLIT: the split-KV instantiation (p.splits > 1); the plain one keeps lo = 0
+// and s = 0 as constants and has no part epilogue.
+template <class C, bool SPLIT>
 __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
   constexpr int D = C::D, NQ = C::NQ, BN = C::BN, S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -161,14 +185,21 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
     const int G = gridDim.x, c = blockIdx.x;
     return r * G + ((r & 1) ? (G - 1 - c) : c);
   };
+  // Item w: query block and head from w / splits, key part s = w % splits.
+  // Part s of a block whose tiles see nf key tiles at most is tiles
+  // [s*nf/splits, (s+1)*nf/splits); nkv[t] counts those tile t sees (may be 0).
   struct Item {
     int q0, bh, nmax;
     int nkv[NQ];
   };
+  struct Part {
+    int s, lo;
+  };
   auto coords = [&](int w) {
     Item it;
     int qb;
-    grouped_order(w, n_qblk, p.BH, p.group, qb, it.bh);
+    const int wb = SPLIT ? w / p.splits : w;
+    grouped_order(wb, n_qblk, p.BH, p.group, qb, it.bh);
     if (p.causal) qb = n_qblk - 1 - qb;
     it.q0 = qb * 128 * NQ;
     it.nmax = 0;
@@ -177,7 +208,35 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
       it.nkv[t] = fwd_kv_tiles(it.q0 + 128 * t, p.N, p.causal, BN);
       it.nmax = max(it.nmax, it.nkv[t]);
     }
+    if constexpr (SPLIT) {
+      const int s = w - wb * p.splits;
+      const int nf = it.nmax;
+      const int lo = (int)((long long)s * nf / p.splits);
+      const int hi = (int)((long long)(s + 1) * nf / p.splits);
+      it.nmax = 0;
+#pragma unroll
+      for (int t = 0; t < NQ; ++t) {
+        it.nkv[t] = max(0, min(hi, it.nkv[t]) - lo);
+        it.nmax = max(it.nmax, it.nkv[t]);
+      }
+    }
     return it;
+  };
+  // Split instantiation: part index s of item w and its first key tile.
+  auto part_of = [&](int w) {
+    Part pt{0, 0};
+    if constexpr (SPLIT) {
+      const int wb = w / p.splits;
+      pt.s = w - wb * p.splits;
+      int qb, bh;
+      grouped_order(wb, n_qblk, p.BH, p.group, qb, bh);
+      if (p.causal) qb = n_qblk - 1 - qb;
+      int nf = 0;
+#pragma unroll
+      for (int t = 0; t < NQ; ++t) nf = max(nf, fwd_kv_tiles(qb * 128 * NQ + 128 * t, p.N, p.causal, BN));
+      pt.lo = (int)((long long)pt.s * nf / p.splits);
+    }
+    return pt;
   };
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
@@ -200,6 +259,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           const int w = item_of(r);
           if (w >= p.items) break;
           const Item I = coords(w);
+          const Part P = part_of(w);
           if constexpr (C::QT) {
             // K(0), then K(j+1) ahead of V(j): the order in which the MMAs read them.
             auto load = [&](const CUtensorMap* m, int j) -> bool {
@@ -208,9 +268,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
               mbar_expect_tx(BAR(C::B_KVFULL + s), C::KV_TILE);
               for (int pn = 0; pn < C::PANELS; ++pn)
                 tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m, BAR(C::B_KVFULL + s),
-                            64 * pn, j * BN, I.bh);
+                            64 * pn, (P.lo + j) * BN, I.bh);
               if (j + C::PREFETCH < I.nmax)
-                for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(m, 64 * pn, (j + C::PREFETCH) * BN, I.bh);
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                  tma_prefetch_l2_3d(m, 64 * pn, (P.lo + j + C::PREFETCH) * BN, I.bh);
               ++it;
               return true;
             };
@@ -221,6 +282,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
             }
             continue;
           }
+          if (SPLIT && I.nmax == 0) continue;  // an empty key part: nothing to load or compute
           // The previous item's S MMAs must be done reading Q.
           if (!wait_one(BAR(C::B_QEMPTY), (nitems & 1) ^ 1, ab, (kKFwd << 8) | 10)) break;
           mbar_expect_tx(BAR(C::B_QFULL), NQ * C::Q_TILE);
@@ -240,11 +302,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
               const CUtensorMap* m = wkv ? &p.v_map : &p.k_map;
               for (int pn = 0; pn < C::PANELS; ++pn)
                 tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m, BAR(C::B_KVFULL + s),
-                            64 * pn, j * BN, I.bh);
+                            64 * pn, (P.lo + j) * BN, I.bh);
               // Pull K/V tiles a few steps beyond the ring into L2.
               if (j + C::PREFETCH < I.nmax)
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                  tma_prefetch_l2_3d(m, 64 * pn, (j + C::PREFETCH) * BN, I.bh);
+                  tma_prefetch_l2_3d(m, 64 * pn, (P.lo + j + C::PREFETCH) * BN, I.bh);
               ++it;
             }
           }
@@ -295,10 +357,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
             const int w = item_of(r);
             if (w >= p.items) break;
             const Item I = coords(w);
+            // An empty key part has no Q hand-off (the softmax warps skip it too).
+            if (I.nmax <= 0) continue;
             // The softmax warps have written this item's Q into TMEM.
             if (!wait_warp(BAR(C::B_QREADY), nitems & 1, ab, (kKFwd << 8) | 11)) break;
             ++nitems;
-            if (I.nmax <= 0) continue;
             int sk = 0;
             if (!take(sk)) break;
             tc_fence_after();
@@ -350,6 +413,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           const int w = item_of(r);
           if (w >= p.items) break;
           const Item I = coords(w);
+          if (SPLIT && I.nmax == 0) continue;  // an empty key part (the producer loaded nothing)
           ok = wait_warp(BAR(C::B_QFULL), nitems & 1, ab, (kKFwd << 8) | 2);
           ++nitems;
           if (!ok) break;
@@ -456,11 +520,26 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
         __syncwarp();
         if (lane == 0) mbar_arrive(BAR(C::B_QREADY));
       };
+      // QT: the first item at or after round r with key tiles (-1 if none).  Q is
+      // written only for those: one QREADY phase per item the issuer waits for, so
+      // the barrier never runs two phases ahead of its waiter.
+      auto next_work = [&](int r0) -> int {
+        if constexpr (!SPLIT) return item_of(r0) < p.items ? item_of(r0) : -1;
+        for (int r2 = r0;; ++r2) {
+          const int w2 = item_of(r2);
+          if (w2 >= p.items) return -1;
+          if (coords(w2).nmax > 0) return w2;
+        }
+      };
       for (int rr = 0; ok; ++rr) {
         const int w = item_of(rr);
         if (w >= p.items) break;
-        if (C::QT && rr == 0) write_q(w);
+        if (C::QT && rr == 0) {
+          const int wq = next_work(0);
+          if (wq >= 0) write_q(wq);
+        }
         const Item I = coords(w);
+        const Part P = part_of(w);
         const int qi = I.q0 + 128 * t + r;
         const int n = I.nkv[t];
         const int bh = I.bh;
@@ -482,7 +561,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           for (int c = 0; c < BN; c += 32) tmem_ld_32x32b_x32(tS + c, sr + c);
           tmem_wait_ld();
           reg_fence<BN>(sr);
-          const int kbase = j * BN;
+          const int kbase = (P.lo + j) * BN;
           if (kbase + BN - 1 > limit) {
 #pragma unroll
             for (int c = 0; c < BN; ++c)
@@ -552,9 +631,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(C::B_PREADY + sb));
         }
-        if (C::QT && ok) {
-          const int wn = item_of(rr + 1);
-          if (wn < p.items) write_q(wn);
+        if (C::QT && ok && I.nmax > 0) {
+          const int wn = next_work(rr + 1);
+          if (wn >= 0) write_q(wn);
         }
         if (ok && n > 0) {
           if (!wait_warp(BAR(C::B_OREADY + oready_bar(g + n - 1)), oready_phase(g + n - 1), ab, (kKFwd << 8) | 9)) {
@@ -562,39 +641,80 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
             break;
           }
           tc_fence_after();
-          const float inv = 1.f / l;
           const bool store = qi < p.N;
           // Staged through this warp's 2 KB of shared memory, 32 columns at a
           // time: each thread writes its row, then each warp store covers 8 rows
           // x 64 contiguous bytes instead of 32 rows x 16 bytes.
           uint8_t* epi = gbase + C::OFF_EPI + (t * 4 + quad) * 2048;
           const int row0 = I.q0 + 128 * t + quad * 32;  // this warp's first query row
-          uint16_t* obase = p.o + ((size_t)bh * p.N + (size_t)row0) * p.dv;
+          if constexpr (!SPLIT) {
+            const float inv = 1.f / l;
+            uint16_t* obase = p.o + ((size_t)bh * p.N + (size_t)row0) * p.dv;
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t orr[32];
-            tmem_ld_32x32b_x32(tO + c0, orr);
-            tmem_wait_ld();
-            reg_fence<32>(orr);
-            uint32_t pk[16];
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t orr[32];
+              tmem_ld_32x32b_x32(tO + c0, orr);
+              tmem_wait_ld();
+              reg_fence<32>(orr);
+              uint32_t pk[16];
 #pragma unroll
-            for (int e = 0; e < 32; e += 2)
-              pk[e >> 1] = pack_bf16(__uint_as_float(orr[e]) * inv, __uint_as_float(orr[e + 1]) * inv);
+              for (int e = 0; e < 32; e += 2)
+                pk[e >> 1] = pack_bf16(__uint_as_float(orr[e]) * inv, __uint_as_float(orr[e + 1]) * inv);
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
-              *reinterpret_cast<uint4*>(epi + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) =
-                  make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-            __syncwarp();
+              for (int u = 0; u < 4; ++u)
+                *reinterpret_cast<uint4*>(epi + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) =
+                    make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+              __syncwarp();
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int rr = j * 8 + (lane >> 2), u = lane & 3;
-              const uint4 val = *reinterpret_cast<const uint4*>(epi + rr * 64 + ((u ^ ((rr >> 1) & 3)) << 4));
-              if (row0 + rr < p.N && c0 + 8 * u < p.dv)
-                *reinterpret_cast<uint4*>(obase + (size_t)rr * p.dv + c0 + 8 * u) = val;
+              for (int j = 0; j < 4; ++j) {
+                const int rr = j * 8 + (lane >> 2), u = lane & 3;
+                const uint4 val = *reinterpret_cast<const uint4*>(epi + rr * 64 + ((u ^ ((rr >> 1) & 3)) << 4));
+                if (row0 + rr < p.N && c0 + 8 * u < p.dv)
+                  *reinterpret_cast<uint4*>(obase + (size_t)rr * p.dv + c0 + 8 * u) = val;
+              }
+              __syncwarp();
             }
-            __syncwarp();
+            if (store) p.lse[(size_t)bh * p.N + qi] = (m_used + log2f(l)) * kLn2;
+          } else {
+            // Part s of a split-KV pass: fp32 O / l and the log2-domain L_s, staged
+            // 16 columns (64 bytes per row) at a time.  A row that sees no key of
+            // the part (l = 0) gets O_s = 0 and L_s = -inf.
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            float* pbase = p.opart + (((size_t)P.s * p.BH + bh) * p.N + (size_t)row0) * p.dv;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t orr[32];
+              tmem_ld_32x32b_x32(tO + c0, orr);
+              tmem_wait_ld();
+              reg_fence<32>(orr);
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                  const int e = 16 * h + 4 * u;
+                  *reinterpret_cast<float4*>(epi + lane * 64 + ((u ^ ((lane >> 1) & 3)) << 4)) =
+                      make_float4(__uint_as_float(orr[e]) * inv, __uint_as_float(orr[e + 1]) * inv,
+                                  __uint_as_float(orr[e + 2]) * inv, __uint_as_float(orr[e + 3]) * inv);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                  const int rr = jj * 8 + (lane >> 2), u = lane & 3;
+                  const float4 val =
+                      *reinterpret_cast<const float4*>(epi + rr * 64 + ((u ^ ((rr >> 1) & 3)) << 4));
+                  const int col = c0 + 16 * h + 4 * u;
+                  if (row0 + rr < p.N && col < p.dv)
+                    *reinterpret_cast<float4*>(pbase + (size_t)rr * p.dv + col) = val;
+                }
+                __syncwarp();
+              }
+            }
+            if (store)
+              p.lpart[((size_t)P.s * p.BH + bh) * p.N + qi] = l > 0.f ? m_used + log2f(l) : -INFINITY;
           }
-          if (store) p.lse[(size_t)bh * p.N + qi] = (m_used + log2f(l)) * kLn2;
+        } else if (SPLIT && ok && qi < p.N) {
+          // This query tile sees no key tile of the part.
+          p.lpart[((size_t)P.s * p.BH + bh) * p.N + qi] = -INFINITY;
         }
         g += n;
       }
@@ -607,6 +727,51 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
     tc_fence_after();
     tmem_dealloc(tmem, C::TMEM_COLS);
   }
+}
+
+// Merge of the split-KV parts: one thread per 8 columns of a row.  Each thread
+// reads the row's `splits` values of L_s (cached), so no shuffles are needed.
+// A part with L_s = -inf saw no key of the row and is skipped (its O_s is
+// not read).  Skipped entirely if a kernel gave up a wait.
+__global__ void __launch_bounds__(256) fwd_merge_kernel(const __grid_constant__ FwdMergeParams p) {
+  grid_dep_wait();
+  if (*reinterpret_cast<volatile const int*>(p.err) != 0) return;
+  const int tpr = p.dv / 8;
+  const long long g = (long long)blockIdx.x * 256 + threadIdx.x;
+  const long long row = g / tpr;
+  if (row >= p.rows) return;
+  const int c = (int)(g - row * tpr) * 8;
+  float mx = -INFINITY;
+  for (int s = 0; s < p.splits; ++s) mx = fmaxf(mx, p.lpart[(size_t)s * p.rows + row]);
+  float wsum = 0.f;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (mx != -INFINITY) {
+    for (int s = 0; s < p.splits; ++s) {
+      const float ls = p.lpart[(size_t)s * p.rows + row];
+      if (ls == -INFINITY) continue;
+      const float wt = exp2f(ls - mx);
+      wsum += wt;
+      const float* src = p.opart + ((size_t)s * p.rows + row) * p.dv + c;
+      const float4 a = *reinterpret_cast<const float4*>(src);
+      const float4 b = *reinterpret_cast<const float4*>(src + 4);
+      acc[0] += wt * a.x;
+      acc[1] += wt * a.y;
+      acc[2] += wt * a.z;
+      acc[3] += wt * a.w;
+      acc[4] += wt * b.x;
+      acc[5] += wt * b.y;
+      acc[6] += wt * b.z;
+      acc[7] += wt * b.w;
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  uint4 out;
+  out.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+  out.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+  out.z = pack_bf16(acc[4] * inv, acc[5] * inv);
+  out.w = pack_bf16(acc[6] * inv, acc[7] * inv);
+  *reinterpret_cast<uint4*>(p.o + (size_t)row * p.dv + c) = out;
+  if (c == 0) p.lse[row] = wsum > 0.f ? (mx + log2f(wsum)) * kLn2 : -INFINITY;
 }
 
 }  // namespace fa

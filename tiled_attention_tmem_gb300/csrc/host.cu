@@ -178,7 +178,34 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
   if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return FA_ERR_MISALIGNED;
-  return run_fwd(q, k, v, o, lse, B * H, N, d, scale, causal, (cudaStream_t)stream);
+  return run_fwd(q, k, v, o, lse, B * H, N, d, scale, causal, 1, nullptr, (cudaStream_t)stream);
+}
+
+size_t fa_fwd_splitkv_workspace_size(int B, int H, int N, int d, int splits) {
+  if (B < 0 || H < 0 || N < 0 || !supported_d(d)) return 0;
+  if (splits < 1 || splits > FA_FWD_MAX_SPLITS) return 0;
+  return splitkv_workspace_bytes(B * H, N, d, splits);
+}
+
+int fa_fwd_choose_splits(int B, int H, int N, int d, int causal) {
+  if (validate_common(B, H, N, d, 1.f, causal) != FA_OK || (long long)B * H * N == 0) return 1;
+  return choose_splits(B * H, N, d, causal);
+}
+
+fa_status fa_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                         int N, int d, float scale, int causal, int splits, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  fa_status s = validate_common(B, H, N, d, scale, causal);
+  if (s != FA_OK) return s;
+  if (splits < 1 || splits > FA_FWD_MAX_SPLITS) return FA_ERR_INVALID_ARG;
+  if ((long long)B * H * N == 0) return FA_OK;
+  if (!q || !k || !v || !o || !lse) return FA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return FA_ERR_MISALIGNED;
+  if (splits > 1 && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+                     workspace_bytes < splitkv_workspace_bytes(B * H, N, d, splits)))
+    return FA_ERR_WORKSPACE;
+  return run_fwd(q, k, v, o, lse, B * H, N, d, scale, causal, splits, workspace, (cudaStream_t)stream);
 }
 
 size_t fa_bwd_workspace_size(int B, int H, int N, int d, int variant) {
@@ -300,6 +327,7 @@ const char* fa_kernel_name(int kind) {
     case FA_KERNEL_BWD_CONV: return "bwd_conv";
     case FA_KERNEL_BWD_KV7: return "bwd_kv7";
     case FA_KERNEL_BWD_Q7: return "bwd_q7";
+    case FA_KERNEL_FWD_MERGE: return "fwd_merge";
   }
   return "unknown";
 }
@@ -307,6 +335,11 @@ const char* fa_kernel_name(int kind) {
 int fa_fwd_launches(int B, int H, int N, int d) {
   if ((long long)B * H * N <= 0 || !supported_d(d)) return 0;
   return fwd_launch_count(d);
+}
+
+int fa_fwd_splitkv_launches(int B, int H, int N, int d, int splits) {
+  if ((long long)B * H * N <= 0 || !supported_d(d) || splits < 1 || splits > FA_FWD_MAX_SPLITS) return 0;
+  return fwd_launch_count(d) + (splits > 1 ? 1 : 0);
 }
 
 int fa_bwd_launches(int B, int H, int N, int d, int variant, int causal) {

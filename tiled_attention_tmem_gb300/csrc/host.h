@@ -68,9 +68,16 @@ fa_status launch(int kind, Kernel kernel, dim3 grid, dim3 block, size_t smem, cu
   return FA_OK;
 }
 
-// Forward launcher (fwd.cu).  Arguments already validated.
+// Forward launcher (fwd.cu).  Arguments already validated.  splits > 1 runs the
+// split-KV form: `workspace` (splitkv_workspace_bytes, 256-byte aligned) holds
+// the fp32 parts at offset 0 and their log-sum-exps at splitkv_lse_offset.
 fa_status run_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N,
-                  int d, float scale, int causal, cudaStream_t st);
+                  int d, float scale, int causal, int splits, void* workspace, cudaStream_t st);
+constexpr int kMaxSplits = 16;
+size_t splitkv_lse_offset(int BH, int N, int d, int splits);
+size_t splitkv_workspace_bytes(int BH, int N, int d, int splits);
+// Parts per query block that the split-KV cost model predicts fastest (1: no split).
+int choose_splits(int BH, int N, int d, int causal);
 int fwd_launch_count(int d);
 
 // Head dims the kernels support and the head dim (64, 128 or 256) whose

@@ -81,6 +81,10 @@ CAUSAL_2K = Workload("b4_h16_n2048_d128_causal", 4, 16, 2048, 128, True, seed=2)
 KSHIFT_8K = Workload("b2_h16_n8192_d128_kshift3", 2, 16, 8192, 128, False, seed=3, k_shift=3.0)
 HDIM256_4K = Workload("b2_h8_n4096_d256_causal_sigma0.5", 2, 8, 4096, 256, True,
                       seed=4, sigma=0.5, scale=1.0 / 16.0)
+# One long head: fewer query blocks than SMs, the case the split-KV forward serves.
+LONG_1H_16K = Workload("b1_h1_n16384_d128_causal", 1, 1, 16384, 128, True, seed=5)
+LONG_1H_8K_D256 = Workload("b1_h1_n8192_d256_causal_sigma0.5", 1, 1, 8192, 256, True,
+                           seed=6, sigma=0.5, scale=1.0 / 16.0)
 
 
 def sweep_workloads() -> list[Workload]:
@@ -109,7 +113,8 @@ def head_dim_workloads() -> list[Workload]:
     return out
 
 
-WORKLOADS = {w.name: w for w in [TINY, CAUSAL_2K, KSHIFT_8K, HDIM256_4K] + sweep_workloads() + head_dim_workloads()}
+WORKLOADS = {w.name: w for w in [TINY, CAUSAL_2K, KSHIFT_8K, HDIM256_4K, LONG_1H_16K, LONG_1H_8K_D256]
+             + sweep_workloads() + head_dim_workloads()}
 
 
 @dataclass
