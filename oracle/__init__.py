@@ -11,7 +11,9 @@ Modules
 -------
 attention       the plain definition: materialised S and P, analytic gradients
 online_softmax  the blockwise m/l merge the tiled method relies on, written as a
-                separate routine so tests can check it against the definition
+                separate routine so tests can check it against the definition, and
+                the split-KV route (parts finished on their own, then merged by
+                their log-sum-exps)
 
 Every function in these modules is pinned by CPU tests (``-m "not gpu"``) to
 closed forms, invariants, brute force on tiny inputs and central finite
@@ -27,7 +29,7 @@ from .attention import (
     backward_parts,
     visible_keys,
 )
-from .online_softmax import blockwise_forward, merge_partials
+from .online_softmax import blockwise_forward, merge_partials, split_forward
 
 __all__ = [
     "scores",
@@ -39,4 +41,5 @@ __all__ = [
     "visible_keys",
     "blockwise_forward",
     "merge_partials",
+    "split_forward",
 ]

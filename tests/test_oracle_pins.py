@@ -79,6 +79,94 @@ def test_random_partitions_merge():
         np.testing.assert_allclose(lse, lse_ref[0, 0], rtol=1e-12, atol=1e-13)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n,parts", [
+    (64, [32, 32]), (64, [16] * 4), (70, [7] * 10), (64, [64]), (65, [0, 30, 0, 35, 0]),
+    (200, [128, 72]), (33, [1, 31, 1]), (256, [64] * 4), (5, [1] * 5),
+])
+def test_split_forward_equals_direct(causal, n, parts):
+    """Key ranges finished on their own and merged by their log-sum-exps give the
+    direct softmax; under the causal mask later ranges are fully masked for the
+    early rows (L_s = -inf, weight 0), and empty ranges contribute nothing."""
+    d = 8
+    q, k, v = rand(n, d), rand(n, d), rand(n, d)
+    o_ref, lse_ref = A.forward(q[None, None], k[None, None], v[None, None], 0.3, causal)
+    o, lse = oracle.split_forward(q, k, v, 0.3, causal, parts)
+    np.testing.assert_allclose(o, o_ref[0, 0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, lse_ref[0, 0], rtol=1e-12, atol=1e-13)
+    o_b, lse_b = oracle.blockwise_forward(q, k, v, 0.3, causal, [p for p in parts if p])
+    np.testing.assert_allclose(o, o_b, rtol=1e-12, atol=1e-13)
+
+
+def test_split_forward_far_apart_maxima_and_random_parts():
+    """Part maxima more than 30 apart (keys shifted along q), and random partitions."""
+    rng = np.random.default_rng(21)
+    n, d = 96, 4
+    q = np.abs(rand(n, d, rng=rng)) + 0.5
+    k = rand(n, d, rng=rng)
+    k[48:] += 20.0  # the second half of the keys scores far higher for every query
+    v = rand(n, d, rng=rng)
+    s = A.scores(q[None, None], k[None, None], 1.0, False)[0, 0]
+    assert np.min(s[:, 48:].max(1) - s[:, :48].max(1)) > 30.0
+    for causal in (False, True):
+        o_ref, lse_ref = A.forward(q[None, None], k[None, None], v[None, None], 1.0, causal)
+        for parts in ([48, 48], [8] * 12, [95, 1], [1, 95]):
+            o, lse = oracle.split_forward(q, k, v, 1.0, causal, parts)
+            np.testing.assert_allclose(o, o_ref[0, 0], rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(lse, lse_ref[0, 0], rtol=1e-12)
+    for trial in range(12):
+        n = int(rng.integers(2, 80))
+        cuts = sorted(rng.integers(0, n + 1, size=int(rng.integers(1, 7))).tolist())
+        edges = [0] + cuts + [n]
+        parts = [b - a for a, b in zip(edges[:-1], edges[1:])]
+        q, k, v = rand(n, 3, rng=rng), rand(n, 3, rng=rng), rand(n, 3, rng=rng)
+        causal = bool(trial % 2)
+        o_ref, lse_ref = A.forward(q[None, None], k[None, None], v[None, None], 0.9, causal)
+        o, lse = oracle.split_forward(q, k, v, 0.9, causal, parts)
+        np.testing.assert_allclose(o, o_ref[0, 0], rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(lse, lse_ref[0, 0], rtol=1e-12, atol=1e-13)
+
+
+def test_split_merge_mistakes_are_caught():
+    """Plausible mistakes in the part merge fail the equality with the direct
+    definition: weights not renormalised by their sum, part LSEs in log2 mixed
+    with natural exponentials, and a fully masked part given weight exp(0)."""
+    n, d = 64, 6
+    q, k, v = rand(n, d), rand(n, d), rand(n, d)
+    o_ref, lse_ref = A.forward(q[None, None], k[None, None], v[None, None], 0.4, True)
+    parts = [(0, 32), (32, 64)]
+    rows = np.arange(n)[:, None]
+    o_s, l_s = [], []
+    for a, b in parts:
+        s = 0.4 * q @ k[a:b].T
+        s = np.where(np.arange(a, b)[None, :] <= rows, s, -np.inf)
+        m = s.max(1)
+        seen = ~np.isneginf(m)
+        p = np.exp(s - np.where(seen, m, 0.0)[:, None])
+        l = p.sum(1)
+        o = np.zeros((n, d))
+        o[seen] = (p @ v[a:b])[seen] / l[seen][:, None]
+        o_s.append(o)
+        l_s.append(np.where(seen, np.where(seen, m, 0.0) + np.log(np.where(seen, l, 1.0)), -np.inf))
+    L = np.stack(l_s)
+    top = L.max(0)
+
+    def merged(w):
+        return np.einsum("sr,srd->rd", w, np.stack(o_s))
+
+    w_ok = np.where(np.isneginf(L), 0.0, np.exp(L - top))
+    good = merged(w_ok / w_ok.sum(0))
+    np.testing.assert_allclose(good, o_ref[0, 0], rtol=1e-12, atol=1e-13)
+    not_renormalised = merged(w_ok)
+    assert np.max(np.abs(not_renormalised - o_ref[0, 0])) > 1e-3
+    w_log2 = np.where(np.isneginf(L), 0.0, np.exp((L - top) / math.log(2.0)))
+    log2_mixup = merged(w_log2 / w_log2.sum(0))
+    assert np.max(np.abs(log2_mixup - o_ref[0, 0])) > 1e-3
+    w_masked_one = np.where(np.isneginf(L), 1.0, np.exp(L - top))
+    masked_weighted = merged(w_masked_one / w_masked_one.sum(0))
+    assert np.max(np.abs(masked_weighted - o_ref[0, 0])) > 1e-3
+
+
 def test_merge_partials_split_kv():
     """Two halves of the keys merged with the m/l algebra equal the whole."""
     n, d = 40, 6
