@@ -7,6 +7,8 @@ any CUDA work is issued.
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -209,3 +211,49 @@ def test_bwd_noalloc_validation(lib):
     big = dict(B=64, H=64, N=8192)
     assert call(d=128, variant=b.FA_BWD_7GEMM, **big) == b.FA_ERR_WORKSPACE
     assert call(d=128, variant=b.FA_BWD_5GEMM, **big) == b.FA_ERR_WORKSPACE
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <stddef.h>
+#include "fa.h"
+
+/* A C caller of the boundary: only calls that are rejected or answered before
+   any CUDA work is issued. */
+int main(void) {
+  int fails = 0;
+  fa_profile prof;
+  if (fa_fwd(NULL, NULL, NULL, NULL, NULL, 1, 1, 128, 80, 0.125f, 0, NULL) != FA_ERR_UNSUPPORTED) fails |= 1;
+  if (fa_fwd(NULL, NULL, NULL, NULL, NULL, 1, 1, 0, 64, 0.125f, 0, NULL) != FA_OK) fails |= 2;
+  if (fa_fwd_splitkv(NULL, NULL, NULL, NULL, NULL, 1, 1, 128, 64, 0.125f, 0, 0, NULL, 0, NULL)
+      != FA_ERR_INVALID_ARG) fails |= 4;
+  if (fa_bwd(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 1, 1, 128, 64, 0.125f, 0, 9, NULL, 0, NULL)
+      != FA_ERR_INVALID_ARG) fails |= 8;
+  if (fa_bwd_workspace_size(1, 1, 128, 100, FA_BWD_AUTO) != 0) fails |= 16;
+  if (fa_fwd_splitkv_workspace_size(1, 1, 128, 64, 2) != (size_t)(4 * 2 * 128 * 64 + 4 * 2 * 128)) fails |= 32;
+  if (fa_strerror(FA_ERR_WORKSPACE) == NULL || fa_kernel_name(FA_KERNEL_FWD_MERGE) == NULL) fails |= 64;
+  if (fa_fwd_splitkv_launches(1, 1, 128, 64, 2) != 2 || fa_fwd_launches(1, 1, 128, 64) != 1) fails |= 128;
+  if (sizeof(prof.launches) / sizeof(prof.launches[0]) != FA_KERNEL_KINDS) fails |= 256;
+  printf("%d\n", fails);
+  return fails != 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_a_c_program_links_the_library(lib, tmp_path):
+    """include/fa.h compiles as strict C99, and a C program linked against the
+    shared library gets the documented answers from calls that launch nothing."""
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(b.LIB_PATH)
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        f"-I{os.path.join(ROOT, 'include')}", str(src), "-o", str(exe),
+                        f"-L{libdir}", "-l:libfa_gb300.so", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert out.returncode == 0 and out.stdout.strip() == "0", out.stdout + out.stderr
