@@ -11,12 +11,16 @@ namespace {
 // dK/dV kernel configurations <d, query rows per step, with dQ, d split, query stages, separate P/dS>.
 // d = 128 5-GEMM: bulk dQ reductions from a shared-memory tile measured faster than per-element
 // or 16-byte reductions straight from registers, worth giving up one query stage.
+// d = 64 5-GEMM: 128 query columns per step over two compute warpgroups, each packing its P^T / dS^T
+// into its own S^T / dP^T columns.
 using KV5_64 = BwdKVCfg<64, 128, true, 1, 2, false>;
 using KV5_128 = BwdKVCfg<128, 64, true, 1, 3, true>;
 using KV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
 using KV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
 // d = 192: dV and dK for all 192 columns fit TMEM next to S and dP, so no d split.
 using KV7_192 = BwdKVCfg<192, 64, false, 1, 2, false>;
+// d = 256: V in TMEM, and the outputs split (a dV item and a dK item per key tile, each with one
+// 256-column accumulator).
 using KV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true, true>;
 // dQ kernel configurations <d, keys per tile, K/V ring slots>.
 using Q7_64 = BwdQCfg<64, 128, 6>;

@@ -190,9 +190,9 @@ struct BwdKVCfg {
   // EARLY: the compute warps load all of S^T / dP^T into registers and release
   // those TMEM columns at once, so S^T(i+1), dP^T(i+1) run during the softmax of i.
   static constexpr bool EARLY = SEP && BM == 64;
-  // Compute warpgroups: the 5-GEMM EARLY kernel splits the BM query columns
-  // (and the dV / dK epilogue) over two warpgroups to halve the per-tile
-  // critical path; the 7-GEMM kernel measured faster with one.
+  // Compute warpgroups: the 5-GEMM kernels (d = 128 with EARLY, and d = 64)
+  // split the BM query columns (and the dV / dK epilogue) over two warpgroups to
+  // halve the per-tile critical path; the 7-GEMM kernels measured faster with one.
   static constexpr int NCW = (DQ && (EARLY || D == 64)) ? 2 : 1;
   static constexpr int CW = BM / NCW;
   // Without separate P^T / dS^T columns, each compute warpgroup packs its results

@@ -23,7 +23,7 @@
 // The MMA issue order S_0(0) S_1(0) PV_0(0) S_0(1) PV_1(0) S_1(1) ... lets the
 // tensor core work on one tile while the other tile's softmax runs.
 //
-// QT (d = 256): Q lives in TMEM (written row by row by the softmax
+// QT (d = 192 and 256): Q lives in TMEM (written row by row by the softmax
 // warps) and S = Q K^T takes A from TMEM, so 64-key tiles run at the full MMA
 // rate and the shared memory holds more K/V slots; each tile's S is
 // double-buffered in TMEM and the order S_t(0) S_t(1) PV_t(0) S_t(2) PV_t(1) ...
