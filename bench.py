@@ -353,6 +353,18 @@ def run_ours(args, rank, world, local_rank):
                  "fwd_frac": fwd_tf / exp_fwd_tf if fwd_tf else None,
                  "bwd_frac": bwd_tf / exp_bwd_tf if bwd_tf else None}
 
+    # The instruction metric of the Metal FlashAttention benchmark quoted in "Potential
+    # algorithmic improvements for backward pass" (head-dim sweep): per visible score,
+    # 2d + 5 instructions in the forward, 3d + 5 in a dQ kernel (S, dP, dQ) and 4d + 5 in a
+    # dK/dV kernel (S, dP, dV, dK), i.e. d multiply-adds per GEMM plus five softmax
+    # instructions; the 5-GEMM kernel runs all five GEMMs (5d + 5).  Giga-instructions/s per
+    # kernel from its measured time, scores halved under the causal mask like the FLOPs.
+    scores = float(w.B * w.H) * w.N * w.N * (0.5 if w.causal else 1.0)
+    per_score = {"fwd": 2 * w.d + 5, "bwd_kv5": 5 * w.d + 5, "bwd_kv7": 4 * w.d + 5, "bwd_q7": 3 * w.d + 5}
+    instr_metric = {name_: per_score[name_] * scores / (kernels[name_]["ms_avg"] / 1e3) / 1e9
+                    for name_ in per_score if name_ in kernels}
+    instr_metric["unit"] = "GINSTRS (per-score instruction counts of the Metal FlashAttention benchmark)"
+
     # The HBM-bound helper kernels against the measured copy bandwidth:
     # algorithmic bytes per launch / average launch time.
     npad = (w.N + 127) // 128 * 128
@@ -460,7 +472,8 @@ def run_ours(args, rank, world, local_rank):
                        "parallelism": "replicas" if world > 1 else "single GPU"},
             "fwd_tflops": fwd_tf, "bwd_tflops": bwd_tf,
             "frac_of_peak": frac, "peak_tflops": float(peaks["bf16_tflops"]),
-            "roofline": roof, "exp_bound": exp_bound, "hbm_kernels": hbm, "cpu_baseline": cpu,
+            "roofline": roof, "exp_bound": exp_bound, "instr_metric": instr_metric, "hbm_kernels": hbm,
+            "cpu_baseline": cpu,
             "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps,
                     "pipelining": "copy in / compute / copy out on three streams, two device buffer sets"},
