@@ -70,3 +70,18 @@ def test_oracle_reached_only_from_the_baseline_reference_and_smoke():
     for path, funcs in allowed.items():
         users = {f for mod, f in _imports(path) if mod.split(".")[0] == "oracle"}
         assert users and users <= funcs, f"{path}: oracle imported in {users}"
+
+
+def test_input_module_holds_no_attention_arithmetic():
+    """The seeded input generators, shared by both sides, draw and round numbers only:
+    no matrix product, exponential, logarithm, maximum or reduction over a tensor."""
+    path = os.path.join(PKG, "inputs.py")
+    tree = ast.parse(open(path, encoding="utf-8").read())
+    banned_calls = {"exp", "exp2", "log", "log2", "max", "maximum", "sum", "matmul", "dot", "einsum",
+                    "tensordot", "softmax", "logsumexp", "amax", "cumsum"}
+    for node in ast.walk(tree):
+        assert not (isinstance(node, ast.BinOp) and isinstance(node.op, ast.MatMult)), "matrix product"
+        if isinstance(node, ast.Call):
+            fn = node.func
+            name = fn.attr if isinstance(fn, ast.Attribute) else getattr(fn, "id", "")
+            assert name not in banned_calls, f"inputs.py calls {name}"
