@@ -27,6 +27,8 @@ from .attention import (
     forward_rows,
     backward,
     backward_parts,
+    backward_rows,
+    row_statistics,
     visible_keys,
 )
 from .online_softmax import blockwise_forward, merge_partials, split_forward
@@ -38,6 +40,8 @@ __all__ = [
     "forward_rows",
     "backward",
     "backward_parts",
+    "backward_rows",
+    "row_statistics",
     "visible_keys",
     "blockwise_forward",
     "merge_partials",

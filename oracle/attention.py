@@ -163,3 +163,66 @@ def backward(q, k, v, do, scale: float, causal: bool):
             dk[b, h] = parts["dK"]
             dv[b, h] = parts["dV"]
     return dq, dk, dv
+
+
+def row_statistics(q, k, v, do, scale: float, causal: bool, b: int, h: int, block: int = 1024):
+    """LSE_i and D_i of every query row of one head, each from its own full score row.
+
+    LSE_i = m_i + ln l_i over the visible keys of row i (the forward's per-row
+    statistic that the backward recomputes P from, "ELI5: FlashAttention",
+    recomputation passage) and D_i = sum_c dO_ic O_ic with O_i = sum_j P_ij V_j.
+    Every row is the definition applied to that row alone; rows are taken
+    ``block`` at a time only to bound memory at long sequences.
+    """
+    qh, kh, vh, doh = (_f64(x[b, h]) for x in (q, k, v, do))
+    n = qh.shape[0]
+    lse = np.empty(n, dtype=np.float64)
+    dd = np.empty(n, dtype=np.float64)
+    cols = np.arange(kh.shape[0])[None, :]
+    for r0 in range(0, n, block):
+        rows = np.arange(r0, min(n, r0 + block))
+        s = scale * (qh[rows] @ kh.T)
+        if causal:
+            s = np.where(cols <= rows[:, None], s, -np.inf)
+        m, l, p = _softmax_stats(s)
+        lse[rows] = (m + np.log(l))[:, 0]
+        dd[rows] = np.sum(doh[rows] * (p @ vh), axis=-1)
+    return lse, dd
+
+
+def backward_rows(q, k, v, do, scale: float, causal: bool, b: int, h: int, qrows, krows):
+    """dQ of chosen query rows and dK, dV of chosen key rows of one head.
+
+    For sequences too long for ``backward_parts``' N x N matrices.  With the
+    per-row statistics of ``row_statistics`` (LSE_i, D_i for every row i):
+
+        P_ij  = exp(s_ij - LSE_i)  (0 where key j is masked for query i)
+        dS_ij = P_ij (dO_i . V_j - D_i)
+        dQ_i  = scale * sum_j dS_ij K_j        for i in qrows (row i of P, dS)
+        dV_j  = sum_i P_ij dO_i                for j in krows (column j of P)
+        dK_j  = scale * sum_i dS_ij Q_i        for j in krows (column j of dS)
+
+    the same gradients as ``backward``, restricted to the chosen rows.
+    Returns (dQ [len(qrows), d], dK [len(krows), d], dV [len(krows), d]).
+    """
+    qh, kh, vh, doh = (_f64(x[b, h]) for x in (q, k, v, do))
+    n = qh.shape[0]
+    lse, dd = row_statistics(q, k, v, do, scale, causal, b, h)
+    qrows = np.asarray(qrows, dtype=np.int64)
+    krows = np.asarray(krows, dtype=np.int64)
+    # Rows of P and dS: query i against every key.
+    s = scale * (qh[qrows] @ kh.T)
+    if causal:
+        s = np.where(np.arange(n)[None, :] <= qrows[:, None], s, -np.inf)
+    p = np.exp(s - lse[qrows, None])
+    ds = p * (doh[qrows] @ vh.T - dd[qrows, None])
+    dq = scale * (ds @ kh)
+    # Columns of P and dS: every query i against key j.
+    st = scale * (qh @ kh[krows].T)
+    if causal:
+        st = np.where(krows[None, :] <= np.arange(n)[:, None], st, -np.inf)
+    pt = np.exp(st - lse[:, None])
+    dst = pt * (doh @ vh[krows].T - dd[:, None])
+    dv = pt.T @ doh
+    dk = scale * (dst.T @ qh)
+    return dq, dk, dv

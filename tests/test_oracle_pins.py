@@ -516,3 +516,78 @@ def test_planted_causal_off_by_one_is_caught():
     assert not np.allclose((p @ v[0, 0])[0], v[0, 0, 0])
     o, _ = A.forward(q, k, v, 0.5, True)
     np.testing.assert_array_equal(o[0, 0, 0], v[0, 0, 0])
+
+
+# ------------------------------------------------------ row-restricted backward
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n,block", [(37, 8), (64, 1024), (1, 4)])
+def test_row_statistics_match_the_definition(causal, n, block):
+    q, k, v, do = (rand(2, 2, n, 5) for _ in range(4))
+    lse, dd = A.row_statistics(q, k, v, do, 0.45, causal, 1, 0, block=block)
+    parts = A.backward_parts(q[1, 0], k[1, 0], v[1, 0], do[1, 0], 0.45, causal)
+    np.testing.assert_allclose(lse, parts["LSE"], rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(dd, parts["D"], rtol=1e-12, atol=1e-13)
+    # D is also rowsum(P o dP), an identity independent of how O was formed.
+    np.testing.assert_allclose(dd, np.sum(parts["P"] * parts["dP"], -1), rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("n", [1, 5, 37, 130])
+def test_backward_rows_match_backward(causal, n):
+    rng = np.random.default_rng(n)
+    q, k, v, do = (rand(2, 3, n, 6, rng=rng) for _ in range(4))
+    k = k + 2.0  # a shifted key set, as in the long-sequence workload
+    dq, dk, dv = A.backward(q, k, v, do, 0.41, causal)
+    rows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, size=7)]))
+    krows = np.unique(np.concatenate([[0, n - 1], rng.integers(0, n, size=5)]))
+    rq, rk, rv = A.backward_rows(q, k, v, do, 0.41, causal, 1, 2, rows, krows)
+    np.testing.assert_allclose(rq, dq[1, 2, rows], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(rk, dk[1, 2, krows], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(rv, dv[1, 2, krows], rtol=1e-10, atol=1e-12)
+
+
+def test_backward_rows_brute_force():
+    n, d = 8, 3
+    q, k, v, do = (rand(n, d) for _ in range(4))
+    for causal in (False, True):
+        _, _, bdq, bdk, bdv = _brute_force(q.tolist(), k.tolist(), v.tolist(), do.tolist(), 0.7, causal)
+        rows = [0, 3, 7]
+        rq, rk, rv = A.backward_rows(q[None, None], k[None, None], v[None, None], do[None, None], 0.7, causal,
+                                     0, 0, rows, rows)
+        np.testing.assert_allclose(rq, np.asarray(bdq)[rows], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(rk, np.asarray(bdk)[rows], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(rv, np.asarray(bdv)[rows], rtol=1e-11, atol=1e-12)
+
+
+def _mutant_backward_rows(kind):
+    """backward_rows with one planted mistake, for the pin below."""
+    def bwd(q, k, v, do, scale, causal, b, h, qrows, krows):
+        qh, kh, vh, doh = (np.asarray(x[b, h], dtype=np.float64) for x in (q, k, v, do))
+        n = qh.shape[0]
+        s_full = A.scores(qh, kh, scale, causal)
+        m = np.max(s_full, -1)
+        lse = m + np.log(np.sum(np.exp(s_full - m[:, None]), -1))
+        if kind == "no_log_l":
+            lse = m  # forgets the ln l term of the log-sum-exp
+        p_full = np.exp(s_full - lse[:, None])
+        dd = np.sum(doh * (p_full @ vh), -1)
+        mask = A.visible_keys(n, causal)
+        if kind == "mask_transposed":
+            mask = mask.T
+        st = np.where(mask[:, krows], scale * (qh @ kh[krows].T), -np.inf)
+        pt = np.exp(st - lse[:, None])
+        dst = pt * (doh @ vh[krows].T - dd[:, None])
+        return None, scale * dst.T @ qh, pt.T @ doh
+    return bwd
+
+
+@pytest.mark.parametrize("kind", ["no_log_l", "mask_transposed"])
+def test_backward_rows_planted_mistakes_are_caught(kind):
+    q, k, v, do = (rand(1, 1, 12, 4) for _ in range(4))
+    causal = kind == "mask_transposed"
+    _, dk, dv = A.backward(q, k, v, do, 0.5, causal)
+    rows = [0, 5, 11]
+    _, mk, mv = _mutant_backward_rows(kind)(q, k, v, do, 0.5, causal, 0, 0, rows, rows)
+    assert not (np.allclose(mk, dk[0, 0, rows], rtol=1e-6) and np.allclose(mv, dv[0, 0, rows], rtol=1e-6))
