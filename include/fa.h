@@ -151,14 +151,38 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  *     accumulator) itself.
  *   - All calls share the array: calls that overlap on the GPU (other streams,
  *     other host threads) race and must be serialised by the caller.
- *   - An expired in-kernel wait is recorded in the array's error word, which
- *     the next call clears; fa_get_device_error does not see it.
+ *   - An expired in-kernel wait is recorded in the array's own error word
+ *     (the later kernels of the call then skip their work, leaving dq, dk, dv
+ *     unwritten).  fa_get_device_error does not see that word: read it with
+ *     fa_bwd_noalloc_device_error after the call, before the next call clears it.
+ *   - With AUTO, a shape whose 5-GEMM scratch exceeds the array runs the 7-GEMM
+ *     form (for example B*H = 64, N = 2048, d = 128 needs 68 MB for 5-GEMM).
  */
 #define FA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dO,
                          const float* lse, void* dq, void* dk, void* dv,
                          int B, int H, int N, int d, float scale, int causal, int variant,
                          void* stream);
+
+/*
+ * Status of the static array's error word used by fa_bwd_noalloc (the pages
+ * have no counterpart: this belongs to the allocation-free entry point above).
+ * Synchronises `stream`; returns FA_ERR_DEVICE_TIMEOUT (and clears the word) if a
+ * bounded in-kernel wait of an fa_bwd_noalloc call on the current device gave
+ * up, FA_ERR_LAUNCH if the CUDA runtime reports an error, else FA_OK.  `site`
+ * (may be NULL) receives (kernel id << 8) | wait site.  Allocates nothing; the
+ * same first-call and overlap rules as fa_bwd_noalloc apply.
+ */
+fa_status fa_bwd_noalloc_device_error(void* stream, int* site);
+
+/*
+ * Self-test of that error word: launches on `stream` one warp whose bounded
+ * wait on a barrier nothing completes gives up after about two seconds and
+ * records FA_ERR_DEVICE_TIMEOUT, site (6 << 8) | 1, in the static array's error
+ * word (as an expired wait inside an fa_bwd_noalloc kernel would).  Touches no
+ * caller memory and allocates nothing.  FA_OK if the launch succeeded.
+ */
+fa_status fa_bwd_noalloc_watchdog_selftest(void* stream);
 
 /* The concrete variant (5 or 7) FA_BWD_AUTO runs for this shape. */
 int fa_bwd_choose(int B, int H, int N, int d, int causal);
@@ -216,6 +240,19 @@ typedef struct {
 int fa_profile_start(void);
 int fa_profile_stop(fa_profile* out);
 const char* fa_kernel_name(int kind);
+
+/*
+ * Throughput probe of the exponential unit (for benchmarks; the pages price the
+ * exponential by its issue rate per SM per clock, "Potential algorithmic
+ * improvements for backward pass", and every exponential of these kernels is one
+ * ex2.approx.ftz.f32).  Launches `blocks` CTAs of 256 threads on `stream`; each
+ * thread evaluates that instruction `iters` times in each of 8 independent
+ * chains and writes one float to sink[blocks * 256] (device memory owned by the
+ * caller).  *count (may be NULL) receives the number of evaluations launched;
+ * time the launch with events on the same stream.  FA_ERR_INVALID_ARG for a NULL
+ * sink or non-positive sizes.
+ */
+fa_status fa_ex2_probe(float* sink, int blocks, int iters, long long* count, void* stream);
 
 /* Number of kernels one fa_fwd / fa_fwd_splitkv / fa_bwd call launches for this shape. */
 int fa_fwd_launches(int B, int H, int N, int d);

@@ -165,7 +165,7 @@ def backward(q, k, v, do, scale: float, causal: bool):
     return dq, dk, dv
 
 
-def row_statistics(q, k, v, do, scale: float, causal: bool, b: int, h: int, block: int = 1024):
+def row_statistics(q, k, v, do, scale: float, causal: bool, b: int, h: int, block: int = 256):
     """LSE_i and D_i of every query row of one head, each from its own full score row.
 
     LSE_i = m_i + ln l_i over the visible keys of row i (the forward's per-row

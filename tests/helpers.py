@@ -54,3 +54,36 @@ def check_grads(got, ref, what=""):
         assert e <= TOL_GRAD_REL * scale, f"{what} {name} max abs err {e:.3e} > {TOL_GRAD_REL}*{scale:.3e}"
         out.append(e / scale if scale else 0.0)
     return out
+
+
+def head_f64(x, b, h):
+    """fp64 copies of Q, K, V, dO of head (b, h) only, shaped [1, 1, N, d] (for the oracle)."""
+    return tuple(I.bf16_bits_to_f64(t[b:b + 1, h:h + 1]) for t in (x.q, x.k, x.v, x.do))
+
+
+class GradCheck:
+    """Collects (got, ref) pieces of dQ, dK, dV from several heads or rows and checks
+    them at the end against one bound per tensor: max abs error <= 2e-2 * max|ref|,
+    with max|ref| taken over everything collected for that tensor (the whole tensor
+    when every element is checked; the sampled elements otherwise, which is stricter).
+    """
+
+    def __init__(self, what=""):
+        self.what = what
+        self.err = [0.0, 0.0, 0.0]
+        self.scale = [0.0, 0.0, 0.0]
+
+    def add(self, got, ref):
+        for t, (g, r) in enumerate(zip(got, ref)):
+            r = np.asarray(r, dtype=np.float64)
+            if r.size == 0:
+                continue
+            self.err[t] = max(self.err[t], max_abs(g, r))
+            self.scale[t] = max(self.scale[t], float(np.max(np.abs(r))))
+
+    def check(self):
+        floor = max(self.scale)
+        for name, e, s in zip(("dQ", "dK", "dV"), self.err, self.scale):
+            scale = s if s > 0 else floor
+            assert e <= TOL_GRAD_REL * scale, f"{self.what} {name} max abs err {e:.3e} > {TOL_GRAD_REL}*{scale:.3e}"
+        return [e / (s if s > 0 else floor) for e, s in zip(self.err, self.scale)]

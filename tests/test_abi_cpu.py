@@ -257,3 +257,14 @@ def test_header_is_plain_c_and_a_c_program_links_the_library(lib, tmp_path):
     assert r.returncode == 0, r.stderr
     out = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert out.returncode == 0 and out.stdout.strip() == "0", out.stdout + out.stderr
+
+
+def test_noalloc_source_calls_no_allocator():
+    """The allocation-free backward's translation unit names no allocating call: no
+    cudaMalloc / cudaFree family, and not the lazily cudaMalloc'ed error word of the
+    workspace entry points."""
+    src = open(os.path.join(ROOT, "tiled_attention_tmem_gb300", "csrc", "bwd_noalloc.cu")).read()
+    code = re.sub(r"//[^\n]*", "", re.sub(r"/\*.*?\*/", "", src, flags=re.S))
+    for banned in ("cudaMalloc", "cudaFree", "cuMemAlloc", "cuMemFree", "device_error_word", "malloc(",
+                   "new ", "std::vector"):
+        assert banned not in code, banned

@@ -39,3 +39,43 @@ def test_split_workspace_size_matches_the_layout():
     r = lambda x: (x + 255) // 256 * 256
     assert api.splitkv_workspace_bytes(B, H, N, d, s) == r(parts) + r(lses)
     assert api.splitkv_workspace_bytes(B, H, N, d, 1) == 0
+
+
+def test_forward_rejects_wrong_shapes():
+    q = _bf16(1, 2, 128, 64)
+    with pytest.raises(ValueError, match="shape"):
+        api.attention_forward(q, _bf16(1, 2, 64, 64), q)
+    with pytest.raises(ValueError, match="shape"):
+        api.attention_forward(_bf16(2, 128, 64), q, q)
+
+
+def test_forward_rejects_a_wrong_out_or_lse():
+    q = _bf16(1, 2, 128, 64)
+    with pytest.raises(ValueError, match="out must have shape"):
+        api.attention_forward(q, q, q, out=_bf16(1, 2, 128, 32))
+    with pytest.raises(ValueError, match="lse must be"):
+        api.attention_forward(q, q, q, lse=torch.zeros((1, 2, 128), dtype=torch.float64))
+    with pytest.raises(ValueError, match="lse must have shape"):
+        api.attention_forward(q, q, q, lse=torch.zeros((1, 2, 64), dtype=torch.float32))
+
+
+def test_backward_rejects_wrong_shapes():
+    q = _bf16(1, 2, 128, 64)
+    lse = torch.zeros((1, 2, 128), dtype=torch.float32)
+    with pytest.raises(ValueError, match="do must have shape"):
+        api.attention_backward(q, q, q, q, _bf16(1, 2, 128, 32), lse)
+    with pytest.raises(ValueError, match="lse must have shape"):
+        api.attention_backward(q, q, q, q, q, torch.zeros((1, 2, 127), dtype=torch.float32))
+    with pytest.raises(ValueError, match="lse must be"):
+        api.attention_backward(q, q, q, q, q, torch.zeros((1, 2, 128), dtype=torch.float16))
+
+
+def test_backward_rejects_wrong_grads_and_workspace():
+    q = _bf16(1, 2, 128, 64)
+    lse = torch.zeros((1, 2, 128), dtype=torch.float32)
+    with pytest.raises(ValueError, match="dk must have shape"):
+        api.attention_backward(q, q, q, q, q, lse, grads=(q, _bf16(1, 2, 128, 16), q))
+    with pytest.raises(ValueError, match="grads must be"):
+        api.attention_backward(q, q, q, q, q, lse, grads=(q, q))
+    with pytest.raises(ValueError, match="workspace must be"):
+        api.attention_backward(q, q, q, q, q, lse, workspace=torch.zeros(16, dtype=torch.float32))

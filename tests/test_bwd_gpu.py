@@ -6,7 +6,7 @@ import pytest
 import oracle
 from tiled_attention_tmem_gb300 import inputs as I
 
-from helpers import check_grads, to_dev, to_f64
+from helpers import GradCheck, check_grads, head_f64, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -107,24 +107,53 @@ def test_five_and_seven_agree():
         assert np.max(np.abs(u64 - w64)) <= 1e-2 * np.max(np.abs(w64))
 
 
-FULL = [I.CAUSAL_2K, I.KSHIFT_8K, I.HDIM256_4K]
+# Full-size workloads in the bench's launch configuration (fa_fwd then fa_bwd on the
+# whole [B, H, N, d] problem), every variant the head dim has.  Every head is checked
+# against the oracle: element by element where its N x N matrices fit (the N = 2048
+# and the d = 256 workloads), and on sampled query rows (dQ) and key rows (dK, dV)
+# computed by the row-restricted oracle for the N = 8192 workload.
+FULL_EVERY_ROW = [I.CAUSAL_2K, I.HDIM256_4K]
 
 
-@pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
-def test_backward_full_size_sampled_heads(w):
-    """Full-size workloads: whole heads (first and last) against the oracle, every variant."""
+@pytest.mark.parametrize("w", FULL_EVERY_ROW, ids=lambda w: w.name)
+def test_backward_full_size_every_head_every_row(w):
     x = I.workload_inputs(w)
-    qf, kf, vf, dof = x.as_f64()
-    heads = [(0, 0), (w.B - 1, w.H - 1)]
     refs = {}
-    for b, h in heads:
-        parts = oracle.backward_parts(qf[b, h], kf[b, h], vf[b, h], dof[b, h], w.softmax_scale, w.causal)
-        refs[(b, h)] = (parts["dQ"], parts["dK"], parts["dV"])
-        del parts
+    for b in range(w.B):
+        for h in range(w.H):
+            qf, kf, vf, dof = head_f64(x, b, h)
+            parts = oracle.backward_parts(qf[0, 0], kf[0, 0], vf[0, 0], dof[0, 0], w.softmax_scale, w.causal)
+            refs[(b, h)] = (parts["dQ"], parts["dK"], parts["dV"])
+            del parts
     for variant in _variants(w.d):
         dq, dk, dv = _fwd_bwd(x, w.B, w.H, w.N, w.d, w.softmax_scale, w.causal, variant)
         g = [to_f64(t) for t in (dq, dk, dv)]
-        for b, h in heads:
-            check_grads([t[b, h] for t in g], refs[(b, h)], f"{w.name} v{variant} b{b} h{h}")
+        chk = GradCheck(f"{w.name} v{variant}")
+        for (b, h), ref in refs.items():
+            chk.add([t[b, h] for t in g], ref)
+        chk.check()
+
+
+def test_backward_full_size_every_head_sampled_rows():
+    """B=2, H=16, N=8192 with keys shifted by +3: every head, sampled rows, both variants."""
+    w = I.KSHIFT_8K
+    x = I.workload_inputs(w)
+    rng = np.random.default_rng(w.seed)
+    refs = {}
+    for b in range(w.B):
+        for h in range(w.H):
+            edge = [0, 127, 128, w.N - 1]
+            qrows = np.unique(np.concatenate([edge, rng.integers(0, w.N, size=20)]))
+            krows = np.unique(np.concatenate([edge, rng.integers(0, w.N, size=20)]))
+            qf, kf, vf, dof = head_f64(x, b, h)
+            refs[(b, h)] = (qrows, krows,
+                            oracle.backward_rows(qf, kf, vf, dof, w.softmax_scale, w.causal, 0, 0, qrows, krows))
+    for variant in _variants(w.d):
+        dq, dk, dv = _fwd_bwd(x, w.B, w.H, w.N, w.d, w.softmax_scale, w.causal, variant)
+        g = [to_f64(t) for t in (dq, dk, dv)]
         for t in g:
             assert np.all(np.isfinite(t))
+        chk = GradCheck(f"{w.name} v{variant}")
+        for (b, h), (qrows, krows, ref) in refs.items():
+            chk.add((g[0][b, h, qrows], g[1][b, h, krows], g[2][b, h, krows]), ref)
+        chk.check()

@@ -1,10 +1,16 @@
-"""Parity on the sequence-sweep configuration: B*N = 16384 tokens, H = 16,
-d in {64, 128}, both masks, N from 512 to 16384 (the shapes and launch
-configuration the sweep measures), checked against the fp64 CPU oracle.
+"""Parity on the sequence sweep and the head-dim sweep, in the launch configuration
+the bench measures (fa_fwd, then fa_bwd with every variant the head dim has, on
+the whole [B, H, N, d] problem), checked against the fp64 CPU oracle.
 
-At each point: the forward on sampled rows of three heads (the oracle computes
-them row by row), and, wherever the oracle's materialised N x N matrices stay
-small (N <= 2048), the backward on whole sampled heads for every variant.
+Sequence sweep: all 24 points (B*N = 16384 tokens, H = 16, N from 512 to 16384,
+d in {64, 128}, both masks).  Head-dim sweep: all 10 points (B = 4, H = 16,
+N = 4096, d in {64, 96, 128, 192, 256}, both masks).
+
+At each point, on sampled heads (the first, the last and one in the middle):
+the forward on sampled rows (computed row by row by the oracle), and the
+backward's dQ on sampled query rows and dK, dV on sampled key rows (the
+row-restricted oracle, which needs no N x N matrix).  Every output element is
+also checked to be finite.
 """
 
 import numpy as np
@@ -13,43 +19,46 @@ import pytest
 import oracle
 from tiled_attention_tmem_gb300 import inputs as I
 
-from helpers import check_fwd, check_grads, to_dev, to_f64
+from helpers import GradCheck, check_fwd, head_f64, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
-SWEEP = {w.name: w for w in I.sweep_workloads()}
-POINTS = ["sweep_n512_d64_causal", "sweep_n512_d128", "sweep_n2048_d64",
-          "sweep_n16384_d64", "sweep_n16384_d128_causal"]
+POINTS = I.sweep_workloads() + I.head_dim_workloads()
 
 
-@pytest.mark.parametrize("name", POINTS)
-def test_sweep_point(name):
+def _variants(d):
+    return (5, 7) if d in (64, 96, 128) else (7,)
+
+
+@pytest.mark.parametrize("w", POINTS, ids=lambda w: w.name)
+def test_sweep_point(w):
+    import torch
+
     from tiled_attention_tmem_gb300 import api
-    w = SWEEP[name]
     x = I.workload_inputs(w)
-    qf, kf, vf, dof = x.as_f64()
     q, k, v, do = (to_dev(t) for t in (x.q, x.k, x.v, x.do))
     o, lse = api.attention_forward(q, k, v, w.softmax_scale, w.causal)
     api.check_device_error()
-    o64, l64 = to_f64(o), to_f64(lse)
-    assert np.all(np.isfinite(o64)) and np.all(np.isfinite(l64))
+    assert bool(torch.isfinite(o).all()) and bool(torch.isfinite(lse).all())
     rng = np.random.default_rng(w.seed)
-    for b, h in [(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 2)]:
-        rows = np.unique(np.concatenate([[0, 1, 127, 128, w.N - 1], rng.integers(0, w.N, size=27)]))
-        o_ref, lse_ref = oracle.forward_rows(qf, kf, vf, w.softmax_scale, w.causal, b, h, rows)
-        check_fwd(o64[b, h, rows], l64[b, h, rows], o_ref, lse_ref, f"{name} b{b} h{h}")
-    if w.N > 2048:
-        return
-    heads = [(0, 0), (w.B - 1, w.H - 1)]
+    heads = sorted({(0, 0), (w.B - 1, w.H - 1), (w.B // 2, w.H // 2)})
+    edge = [0, 1, 127, 128, w.N - 1]
     refs = {}
     for b, h in heads:
-        parts = oracle.backward_parts(qf[b, h], kf[b, h], vf[b, h], dof[b, h], w.softmax_scale, w.causal)
-        refs[(b, h)] = (parts["dQ"], parts["dK"], parts["dV"])
-    for variant in (5, 7):
+        qf, kf, vf, dof = head_f64(x, b, h)
+        rows = np.unique(np.concatenate([edge, rng.integers(0, w.N, size=27)]))
+        o_ref, lse_ref = oracle.forward_rows(qf, kf, vf, w.softmax_scale, w.causal, 0, 0, rows)
+        check_fwd(to_f64(o[b, h])[rows], to_f64(lse[b, h])[rows], o_ref, lse_ref, f"{w.name} b{b} h{h}")
+        qrows = np.unique(np.concatenate([edge, rng.integers(0, w.N, size=11)]))
+        krows = np.unique(np.concatenate([edge, rng.integers(0, w.N, size=11)]))
+        refs[(b, h)] = (qrows, krows,
+                        oracle.backward_rows(qf, kf, vf, dof, w.softmax_scale, w.causal, 0, 0, qrows, krows))
+    for variant in _variants(w.d):
         dq, dk, dv = api.attention_backward(q, k, v, o, do, lse, w.softmax_scale, w.causal, variant=variant)
         api.check_device_error()
-        g = [to_f64(t) for t in (dq, dk, dv)]
-        for b, h in heads:
-            check_grads([t[b, h] for t in g], refs[(b, h)], f"{name} v{variant} b{b} h{h}")
-        for t in g:
-            assert np.all(np.isfinite(t))
+        for t in (dq, dk, dv):
+            assert bool(torch.isfinite(t).all())
+        chk = GradCheck(f"{w.name} v{variant}")
+        for (b, h), (qrows, krows, ref) in refs.items():
+            chk.add((to_f64(dq[b, h])[qrows], to_f64(dk[b, h])[krows], to_f64(dv[b, h])[krows]), ref)
+        chk.check()

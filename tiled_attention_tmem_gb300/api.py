@@ -12,11 +12,24 @@ import math
 from . import binding as _b
 
 
-def _check(t, name, dtype):
+def _validate(specs, device=None):
+    """Rejects any operand that is not a contiguous CUDA tensor of its dtype and
+    shape on one device, before a pointer of it can reach the library.  specs:
+    (tensor, name, dtype, shape or None); dtypes and shapes are checked first."""
     import torch
-    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
-        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
-    return t
+    for t, name, dtype, shape in specs:
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch tensor")
+        if t.dtype != dtype:
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor, not {t.dtype}")
+        if shape is not None and tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name} must have shape {tuple(shape)}, not {tuple(t.shape)}")
+    for t, name, dtype, _ in specs:
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor")
+        dev = device if device is not None else specs[0][0].device
+        if t.device != dev:
+            raise ValueError(f"{name} is on {t.device}, the other operands on {dev}")
 
 
 def _stream(stream):
@@ -33,13 +46,17 @@ def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
     (a uint8 CUDA tensor of ``splitkv_workspace_bytes`` or more) is allocated when
     needed and not given."""
     import torch
-    for t, n in ((q, "q"), (k, "k"), (v, "v")):
-        _check(t, n, torch.bfloat16)
-    if q.dim() != 4 or k.shape != q.shape or v.shape != q.shape:
+    if not isinstance(q, torch.Tensor) or q.dim() != 4:
         raise ValueError("q, k, v must share one [B, H, N, d] shape")
     B, H, N, d = q.shape
+    specs = [(q, "q", torch.bfloat16, None), (k, "k", torch.bfloat16, q.shape), (v, "v", torch.bfloat16, q.shape)]
+    if out is not None:
+        specs.append((out, "out", torch.bfloat16, q.shape))
+    if lse is not None:
+        specs.append((lse, "lse", torch.float32, (B, H, N)))
+    _validate(specs)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
-    o = torch.empty_like(q) if out is None else _check(out, "out", torch.bfloat16)
+    o = torch.empty_like(q) if out is None else out
     l = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     if splits is None:
         splits = _b.fa_fwd_choose_splits(B, H, N, d, int(causal))
@@ -49,9 +66,13 @@ def attention_forward(q, k, v, scale: float | None = None, causal: bool = False,
         if st != _b.FA_OK:
             raise _b.FaError(st, "fa_fwd")
         return o, l
+    need = _b.fa_fwd_splitkv_workspace_size(B, H, N, d, splits)
     if workspace is None:
-        need = _b.fa_fwd_splitkv_workspace_size(B, H, N, d, splits)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    else:
+        _validate([(workspace, "workspace", torch.uint8, None)], q.device)
+        if workspace.numel() < need:
+            raise ValueError(f"workspace holds {workspace.numel()} bytes, {need} are needed")
     st = _b.fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), l.data_ptr(),
                            B, H, N, d, scale, int(causal), splits, workspace.data_ptr(),
                            workspace.numel(), _stream(stream))
@@ -72,14 +93,25 @@ def attention_backward(q, k, v, o, do, lse, scale: float | None = None, causal: 
                        variant: int = _b.FA_BWD_AUTO, workspace=None, grads=None, stream=None):
     """Returns (dQ, dK, dV) bf16 [B,H,N,d]; ``workspace`` is a uint8 CUDA tensor or None."""
     import torch
-    for t, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o"), (do, "do")):
-        _check(t, n, torch.bfloat16)
-    _check(lse, "lse", torch.float32)
+    if not isinstance(q, torch.Tensor) or q.dim() != 4:
+        raise ValueError("q, k, v, o, do must share one [B, H, N, d] shape")
     B, H, N, d = q.shape
+    if grads is not None and len(grads) != 3:
+        raise ValueError("grads must be (dq, dk, dv)")
+    specs = [(q, "q", torch.bfloat16, None)] + [(t, n, torch.bfloat16, q.shape)
+                                                for t, n in ((k, "k"), (v, "v"), (o, "o"), (do, "do"))]
+    specs.append((lse, "lse", torch.float32, (B, H, N)))
+    if grads is not None:
+        specs += [(t, n, torch.bfloat16, q.shape) for t, n in zip(grads, ("dq", "dk", "dv"))]
+    if workspace is not None:
+        specs.append((workspace, "workspace", torch.uint8, None))
+    _validate(specs)
     scale = 1.0 / math.sqrt(d) if scale is None else scale
     need = _b.fa_bwd_workspace_size(B, H, N, d, variant)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    elif workspace.numel() < need:
+        raise ValueError(f"workspace holds {workspace.numel()} bytes, {need} are needed")
     if grads is None:
         grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     dq, dk, dv = grads

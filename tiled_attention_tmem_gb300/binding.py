@@ -43,6 +43,8 @@ SIGNATURES = {
                     _I, _I, _I, _I, _F, _I, _I, _VP, _SZ, _VP]),
     "fa_bwd_noalloc": (_I, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                             _I, _I, _I, _I, _F, _I, _I, _VP]),
+    "fa_bwd_noalloc_device_error": (_I, [_VP, ctypes.POINTER(_I)]),
+    "fa_bwd_noalloc_watchdog_selftest": (_I, [_VP]),
     "fa_bwd_choose": (_I, [_I, _I, _I, _I, _I]),
     "fa_get_device_error": (_I, [_VP, ctypes.POINTER(_I)]),
     "fa_watchdog_selftest": (_I, [_VP]),
@@ -51,6 +53,7 @@ SIGNATURES = {
     "fa_profile_start": (_I, []),
     "fa_profile_stop": (_I, [_VP]),
     "fa_kernel_name": (ctypes.c_char_p, [_I]),
+    "fa_ex2_probe": (_I, [_VP, _I, _I, ctypes.POINTER(ctypes.c_longlong), _VP]),
     "fa_fwd_launches": (_I, [_I, _I, _I, _I]),
     "fa_fwd_splitkv_launches": (_I, [_I, _I, _I, _I, _I]),
     "fa_bwd_launches": (_I, [_I, _I, _I, _I, _I, _I]),
@@ -126,6 +129,17 @@ def fa_bwd_noalloc(q, k, v, o, dO, lse, dq, dk, dv, B, H, N, d, scale, causal, v
 FA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
+def fa_bwd_noalloc_device_error(stream) -> tuple[int, int]:
+    """(status, site) of the no-alloc backward's own error word; reading clears it."""
+    site = _I(0)
+    status = lib().fa_bwd_noalloc_device_error(stream, ctypes.byref(site))
+    return status, site.value
+
+
+def fa_bwd_noalloc_watchdog_selftest(stream) -> int:
+    return lib().fa_bwd_noalloc_watchdog_selftest(stream)
+
+
 def fa_bwd_choose(B, H, N, d, causal) -> int:
     return lib().fa_bwd_choose(B, H, N, d, int(causal))
 
@@ -142,6 +156,13 @@ def fa_watchdog_selftest(stream) -> int:
 
 def fa_last_cuda_error() -> int:
     return lib().fa_last_cuda_error()
+
+
+def fa_ex2_probe(sink, blocks, iters, stream) -> tuple[int, int]:
+    """Launches the exponential-unit probe; returns (status, ex2 evaluations launched)."""
+    count = ctypes.c_longlong(0)
+    status = lib().fa_ex2_probe(sink, blocks, iters, ctypes.byref(count), stream)
+    return status, count.value
 
 
 def fa_fwd_launches(B, H, N, d) -> int:

@@ -44,10 +44,16 @@ def _newest_input_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
+# What the last build_library call did: "compiled" or "reused" (an up-to-date library).
+last_action = ""
+
+
 def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compiles and links the library if any source is newer; returns its path."""
+    global last_action
     if (not force and os.path.exists(LIB_PATH)
             and os.path.getmtime(LIB_PATH) >= _newest_input_mtime()):
+        last_action = "reused"
         return LIB_PATH
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
@@ -74,6 +80,7 @@ def build_library(force: bool = False, verbose: bool = False, ptxas_info: bool =
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
+    last_action = "compiled"
     return LIB_PATH
 
 

@@ -15,7 +15,7 @@ namespace {
 // into its own S^T / dP^T columns.
 using KV5_64 = BwdKVCfg<64, 128, true, 1, 2, false>;
 using KV5_128 = BwdKVCfg<128, 64, true, 1, 3, true>;
-using KV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
+using KV7_64 = BwdKVCfg<64, 128, false, 1, 3, false>;
 using KV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
 // d = 192: dV and dK for all 192 columns fit TMEM next to S and dP, so no d split.
 using KV7_192 = BwdKVCfg<192, 64, false, 1, 2, false>;

@@ -155,7 +155,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
 // Same tile configurations as the workspace-taking backward.
 using NKV5_64 = BwdKVCfg<64, 128, true, 1, 2, false>;
 using NKV5_128 = BwdKVCfg<128, 64, true, 1, 3, true>;
-using NKV7_64 = BwdKVCfg<64, 128, false, 1, 3, true>;
+using NKV7_64 = BwdKVCfg<64, 128, false, 1, 3, false>;
 using NKV7_128 = BwdKVCfg<128, 64, false, 1, 4, true>;
 using NKV7_192 = BwdKVCfg<192, 64, false, 1, 2, false>;
 using NKV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true, true>;
@@ -208,4 +208,27 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
         return run<NKV7_192, NQ7_192, 256>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, false, base, st);
       return run<NKV7_256, NQ7_256, 256>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, false, base, st);
   }
+}
+
+// The error word of the static array: read (and cleared) without allocating.
+extern "C" fa_status fa_bwd_noalloc_device_error(void* stream, int* site) {
+  if (site) *site = 0;
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda_error(e);
+  unsigned char* base = scratch_address();
+  if (!base) return FA_ERR_LAUNCH;
+  int h[2] = {0, 0};
+  e = cudaMemcpy(h, base, sizeof(h), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return record_cuda_error(e);
+  if (h[0] == 0) return FA_OK;
+  if (site) *site = h[1];
+  e = cudaMemset(base, 0, sizeof(h));
+  if (e != cudaSuccess) return record_cuda_error(e);
+  return FA_ERR_DEVICE_TIMEOUT;
+}
+
+extern "C" fa_status fa_bwd_noalloc_watchdog_selftest(void* stream) {
+  unsigned char* base = scratch_address();
+  if (!base) return FA_ERR_LAUNCH;
+  return launch_watchdog_selftest(reinterpret_cast<int*>(base), static_cast<cudaStream_t>(stream));
 }

@@ -14,6 +14,10 @@ int* device_error_word();
 // Records a CUDA runtime error code for fa_last_cuda_error and returns FA_ERR_LAUNCH.
 fa_status record_cuda_error(cudaError_t e);
 
+// Launches the watchdog self-test kernel (one warp whose bounded wait expires)
+// against the given device error word (watchdog.cu).
+fa_status launch_watchdog_selftest(int* err, cudaStream_t st);
+
 // Builds a 3-D TMA descriptor over a contiguous [BH, N, inner] tensor:
 // dims {inner, N, BH}, box {64, box_rows, 1}, 128-byte swizzle, zero fill out of bounds.
 fa_status make_tile_map(CUtensorMap* map, const void* base, CUtensorMapDataType dtype,

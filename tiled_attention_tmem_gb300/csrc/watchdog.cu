@@ -23,12 +23,16 @@ __global__ void __launch_bounds__(32, 1) watchdog_selftest_kernel(int* err) {
   (void)wait_warp(smem_u32(&bar), 0, ab, (kKSelfTest << 8) | 1);
 }
 
+fa_status launch_watchdog_selftest(int* err, cudaStream_t st) {
+  watchdog_selftest_kernel<<<1, 32, 0, st>>>(err);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? FA_OK : record_cuda_error(e);
+}
+
 }  // namespace fa
 
 extern "C" fa_status fa_watchdog_selftest(void* stream) {
   int* err = fa::device_error_word();
   if (!err) return fa::record_cuda_error(cudaErrorMemoryAllocation);
-  fa::watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err);
-  const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? FA_OK : fa::record_cuda_error(e);
+  return fa::launch_watchdog_selftest(err, static_cast<cudaStream_t>(stream));
 }

@@ -24,10 +24,15 @@ import numpy as np
 def f32_to_bf16_bits(x) -> np.ndarray:
     """Round float32 values to bf16 (nearest, ties to even); returns uint16 bit patterns."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    bits = x.view(np.uint32).astype(np.uint64)
-    rounded = (bits + 0x7FFF + ((bits >> 16) & 1)) >> 16
-    nan = np.isnan(x)
+    bits = x.view(np.uint32)
+    # bits + 0x7FFF + lsb, then >> 16: the largest non-NaN pattern (-inf, 0xFF800000)
+    # stays below 2^32, so 32-bit arithmetic does not wrap; NaNs are set afterwards.
+    rounded = (bits >> 16) & 1
+    rounded += bits
+    rounded += 0x7FFF
+    rounded >>= 16
     out = rounded.astype(np.uint16)
+    nan = np.isnan(x)
     if nan.any():
         out[nan] = 0x7FC0
     return out
