@@ -60,6 +60,8 @@ def parse_args():
                     help="forward key parts per query block: 'auto' (the library's cost model) or a count")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--variant-table", action="store_true",
+                    help="time the 5-GEMM and 7-GEMM backward over a grid of shapes (one JSON line per point)")
     ap.add_argument("--min-seconds", type=float, default=1.0,
                     help="repeat the timed pass of K steps until this long has elapsed (median pass reported)")
     return ap.parse_args()
@@ -558,8 +560,71 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
+def variant_grid():
+    """(d, causal, B*H, N) points of the 5-GEMM / 7-GEMM comparison: N from 512 to
+    16384, one to 512 heads, capped at B*H*N^2 <= 2^32 so that a point stays short."""
+    pts = []
+    for d in (64, 96, 128):
+        for causal in (False, True):
+            for n in (512, 1024, 2048, 4096, 8192, 16384):
+                for bh in (1, 2, 4, 8, 16, 32, 64, 128, 256, 512):
+                    if bh * n * n <= 1 << 32:
+                        pts.append((d, causal, bh, n))
+    return pts
+
+
+def run_variant_table(args):
+    """Times fa_bwd with the 5-GEMM and the 7-GEMM form at every point of
+    variant_grid() (CUDA events on the launching stream, L2 flushed between calls,
+    best of --steps calls after --warmup) and prints one JSON line per point with
+    both times and the faster form: the measurements behind fa_bwd_choose."""
+    import torch
+
+    from tiled_attention_tmem_gb300 import api, binding as b, build
+
+    build.build_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    gen = torch.Generator(device=dev)
+    for d, causal, bh, n in variant_grid():
+        gen.manual_seed(1000003 * d + 1009 * n + bh + (7 if causal else 0))
+        shape = (1, bh, n, d)
+        q, k, v, do = (torch.randn(shape, generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                       for _ in range(4))
+        scale = d ** -0.5
+        o, lse = api.attention_forward(q, k, v, scale, causal)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        ws = torch.empty(b.fa_bwd_workspace_size(1, bh, n, d, b.FA_BWD_AUTO), dtype=torch.uint8, device=dev)
+        ms = {}
+        for variant in (b.FA_BWD_5GEMM, b.FA_BWD_7GEMM):
+            best = None
+            for i in range(args.warmup + args.steps):
+                flush.fill_(float(i))
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                api.attention_backward(q, k, v, o, do, lse, scale, causal, variant=variant, workspace=ws,
+                                       grads=grads)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                if i >= args.warmup:
+                    t = e0.elapsed_time(e1)
+                    best = t if best is None else min(best, t)
+            ms[variant] = best
+        api.check_device_error()
+        flops = 10.0 * bh * n * n * d * (0.5 if causal else 1.0)
+        print(json.dumps({"d": d, "causal": causal, "BH": bh, "N": n,
+                          "ms5": ms[5], "ms7": ms[7], "tflops5": flops / ms[5] / 1e9, "tflops7": flops / ms[7] / 1e9,
+                          "faster": 5 if ms[5] <= ms[7] else 7,
+                          "auto": b.fa_bwd_choose(1, bh, n, d, int(causal))}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.variant_table:
+        run_variant_table(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
