@@ -113,6 +113,11 @@ int fa_fwd_choose_splits(int B, int H, int N, int d, int causal);
  *   D (fp32 row dot products dO.O):    4*B*H*Npad bytes
  *   5-GEMM only, fp32 dQ accumulator:  4*B*H*Npad*Dk bytes (Dk = 64 or 128: the
  *                                      kernel head dim, 128 for d = 96)
+ *   query-range split of the dK/dV kernel (shapes with fewer key tiles than
+ *   SMs, chosen by the library's cost model for this shape and variant):
+ *                                      2*4*S*B*H*Npad*Dk bytes of fp32 partial
+ *                                      dK and dV for S parts (Dk: 64, 128 or
+ *                                      256), summed by one extra kernel
  *   work-item counters:                256 bytes
  * with Npad = N rounded up to a multiple of 128.  5-GEMM: d <= 128.
  */
@@ -231,7 +236,8 @@ enum {
   FA_KERNEL_BWD_KV7 = 4,  /* 7-GEMM dK/dV kernel */
   FA_KERNEL_BWD_Q7 = 5,   /* 7-GEMM dQ kernel */
   FA_KERNEL_FWD_MERGE = 6, /* split-KV merge of the forward's parts */
-  FA_KERNEL_KINDS = 7
+  FA_KERNEL_BWD_KVSUM = 7, /* sum of the dK/dV kernel's query-range parts */
+  FA_KERNEL_KINDS = 8
 };
 typedef struct {
   int launches[FA_KERNEL_KINDS];

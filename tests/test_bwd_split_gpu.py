@@ -1,0 +1,83 @@
+"""Query-range split of the dK/dV kernel (few heads, long sequences) against the
+fp64 CPU oracle, through the C ABI.
+
+With fewer key tiles than SMs the library cuts each key tile's query tiles into
+parts, runs each part as its own work item writing fp32 partial dK and dV, and
+adds the parts in a separate kernel.  These shapes are ones where the library's
+cost model splits (checked through the launch count: one extra kernel)."""
+
+import numpy as np
+import pytest
+
+import oracle
+from tiled_attention_tmem_gb300 import binding as b
+from tiled_attention_tmem_gb300 import inputs as I
+
+from helpers import GradCheck, check_grads, head_f64, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+# (B, H, N, d, causal, variant)
+CASES = [
+    (1, 1, 4096, 128, True, 5),
+    (1, 1, 4096, 128, True, 7),
+    (1, 1, 3000, 96, True, 5),
+    (1, 1, 2500, 64, True, 5),
+    (1, 1, 4096, 64, True, 7),
+    (1, 1, 4096, 256, True, 7),
+    (1, 1, 3333, 192, True, 7),
+]
+
+
+def _split_used(B, H, N, d, causal, variant):
+    return b.fa_bwd_launches(B, H, N, d, variant, int(causal)) == 4
+
+
+def _run(x, B, H, N, d, causal, variant):
+    from tiled_attention_tmem_gb300 import api
+    q, k, v, do = (to_dev(t) for t in (x.q, x.k, x.v, x.do))
+    scale = 1.0 / np.sqrt(d)
+    o, lse = api.attention_forward(q, k, v, scale, causal)
+    grads = api.attention_backward(q, k, v, o, do, lse, scale, causal, variant=variant)
+    api.check_device_error()
+    return [to_f64(t) for t in grads]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "b{}h{}n{}d{}{}-v{}".format(*c[:4], "c" if c[4] else "", c[5]))
+def test_split_backward_matches_oracle(case):
+    B, H, N, d, causal, variant = case
+    assert _split_used(B, H, N, d, causal, variant), "the cost model no longer splits this shape"
+    x = I.make_inputs(B, H, N, d, seed=3100 + N + d)
+    got = _run(x, B, H, N, d, causal, variant)
+    qf, kf, vf, dof = head_f64(x, 0, 0)
+    parts = oracle.backward_parts(qf[0, 0], kf[0, 0], vf[0, 0], dof[0, 0], 1.0 / np.sqrt(d), causal)
+    check_grads([t[0, 0] for t in got], (parts["dQ"], parts["dK"], parts["dV"]), f"{case}")
+
+
+def test_split_seven_gemm_is_bitwise_reproducible():
+    B, H, N, d, causal = 1, 1, 4096, 128, True
+    assert _split_used(B, H, N, d, causal, 7)
+    x = I.make_inputs(B, H, N, d, seed=3200)
+    a = _run(x, B, H, N, d, causal, 7)
+    c = _run(x, B, H, N, d, causal, 7)
+    for u, w in zip(a, c):
+        assert np.array_equal(u, w)
+
+
+def test_split_long_single_head_sampled_rows():
+    """One head of 16384 rows under the causal mask (the few-heads workload), both
+    variants, on sampled rows of the row-restricted oracle."""
+    w = I.LONG_1H_16K
+    x = I.workload_inputs(w)
+    rng = np.random.default_rng(w.seed)
+    edge = [0, 127, 128, w.N - 1]
+    qrows = np.unique(np.concatenate([edge, rng.integers(0, w.N, size=40)]))
+    krows = np.unique(np.concatenate([edge, rng.integers(0, w.N, size=40)]))
+    qf, kf, vf, dof = head_f64(x, 0, 0)
+    ref = oracle.backward_rows(qf, kf, vf, dof, w.softmax_scale, w.causal, 0, 0, qrows, krows)
+    for variant in (5, 7):
+        assert _split_used(w.B, w.H, w.N, w.d, w.causal, variant)
+        g = _run(x, w.B, w.H, w.N, w.d, w.causal, variant)
+        chk = GradCheck(f"{w.name} v{variant}")
+        chk.add((g[0][0, 0, qrows], g[1][0, 0, krows], g[2][0, 0, krows]), ref)
+        chk.check()

@@ -177,7 +177,7 @@ def fa_bwd_launches(B, H, N, d, variant, causal=0) -> int:
     return lib().fa_bwd_launches(B, H, N, d, variant, int(causal))
 
 
-FA_KERNEL_KINDS = 7
+FA_KERNEL_KINDS = 8
 
 
 class FaProfile(ctypes.Structure):

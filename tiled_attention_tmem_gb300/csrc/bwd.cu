@@ -1,7 +1,13 @@
 // Backward launchers: workspace carving, tile configurations and TMA descriptors.
 #include "bwd.cuh"
 #include <algorithm>
+#include <functional>
+#include <map>
+#include <mutex>
+#include <queue>
+#include <tuple>
 #include <type_traits>
+#include <vector>
 
 #include "host.h"
 
@@ -34,17 +40,28 @@ struct Workspace {
   float* lse2;
   float* dd;
   float* dqacc;
+  float* dkpart;  // query-range split: fp32 partial dK, dV [qsplit][BH][Npad][d]
+  float* dvpart;
   int* sched;  // work-item counters, in the workspace's last 256 bytes
 };
 
-Workspace carve(void* ws, int BH, int Npad, int d, bool with_dq) {
+Workspace carve(void* ws, int BH, int Npad, int d, bool with_dq, int qsplit) {
   uint8_t* b = static_cast<uint8_t*>(ws);
   const size_t rows = (size_t)BH * Npad;
   Workspace w;
   w.lse2 = reinterpret_cast<float*>(b);
   w.dd = reinterpret_cast<float*>(b + align256(4 * rows));
-  w.dqacc = with_dq ? reinterpret_cast<float*>(b + 2 * align256(4 * rows)) : nullptr;
-  w.sched = reinterpret_cast<int*>(b + 2 * align256(4 * rows) + (with_dq ? 4 * rows * (size_t)d : 0));
+  size_t off = 2 * align256(4 * rows);
+  w.dqacc = with_dq ? reinterpret_cast<float*>(b + off) : nullptr;
+  off += with_dq ? 4 * rows * (size_t)d : 0;
+  w.dkpart = w.dvpart = nullptr;
+  if (qsplit > 1) {
+    const size_t part_bytes = 4 * (size_t)qsplit * rows * d;
+    w.dkpart = reinterpret_cast<float*>(b + off);
+    w.dvpart = reinterpret_cast<float*>(b + off + part_bytes);
+    off += 2 * part_bytes;
+  }
+  w.sched = reinterpret_cast<int*>(b + off);
   return w;
 }
 
@@ -74,7 +91,7 @@ fa_status run_conv(const Workspace& w, void* dq, int BH, int N, int Npad, int hd
 
 template <class C>
 fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, const Workspace& w, void* dk,
-                 void* dv, int BH, int N, int Npad, int hd, float scale, int causal, cudaStream_t st) {
+                 void* dv, int BH, int N, int Npad, int hd, float scale, int causal, int qsplit, cudaStream_t st) {
   BwdKVParams p;
   fa_status s;
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -98,16 +115,24 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
-  p.group = causal ? l2_head_group(12.0 * N * C::D, BH, ((N + C::BN - 1) / C::BN) * C::DSPLIT)
-                   : head_group(((N + C::BN - 1) / C::BN) * C::DSPLIT, BH);
+  const int tiles = ((N + C::BN - 1) / C::BN) * C::DSPLIT * qsplit;
+  p.group = causal ? l2_head_group(12.0 * N * C::D, BH, tiles) : head_group(tiles, BH);
   p.sched = w.sched;
-  const long long items = (long long)((N + C::BN - 1) / C::BN) * BH * C::DSPLIT;
+  p.qsplit = qsplit;
+  p.dkpart = w.dkpart;
+  p.dvpart = w.dvpart;
+  const long long items = (long long)tiles * BH;
   if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.items = (int)items;
   // Persistent grid: one CTA per SM (one fits per SM), each walking its items.
   const long long grid = std::min<long long>(items, sm_count_cached());
-  return launch(C::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<C>, dim3((unsigned)grid),
-                dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  fa_status s2 = launch(C::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<C>, dim3((unsigned)grid),
+                        dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  if (s2 != FA_OK || qsplit <= 1) return s2;
+  KVSumParams sp{w.dkpart, w.dvpart, static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv), p.err,
+                 N, Npad, BH, hd, C::D, qsplit, scale};
+  const long long threads = (long long)BH * N * (hd / 8);
+  return launch(FA_KERNEL_BWD_KVSUM, bwd_kvsum_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, sp);
 }
 
 template <class C>
@@ -150,17 +175,18 @@ fa_status run_d(const void* q, const void* k, const void* v, const void* o, cons
                 cudaStream_t st) {
   const int Npad = (N + 127) / 128 * 128;
   const bool five = variant == FA_BWD_5GEMM;
-  const Workspace w = carve(ws, BH, Npad, D, five);
+  const int qsplit = choose_qsplit(BH, N, hd, causal, variant);
+  const Workspace w = carve(ws, BH, Npad, D, five, qsplit);
   fa_status s = run_pre<D>(o, dO, lse, w, BH, N, Npad, hd, st);
   if (s != FA_OK) return s;
   if (five) {
     if constexpr (!std::is_same<KV5, void>::value) {
-      if ((s = run_kv<KV5>(q, k, v, dO, w, dk, dv, BH, N, Npad, hd, scale, causal, st)) != FA_OK) return s;
+      if ((s = run_kv<KV5>(q, k, v, dO, w, dk, dv, BH, N, Npad, hd, scale, causal, qsplit, st)) != FA_OK) return s;
       return run_conv<D>(w, dq, BH, N, Npad, hd, scale, st);
     }
     return FA_ERR_UNSUPPORTED;
   }
-  if ((s = run_kv<KV7>(q, k, v, dO, w, dk, dv, BH, N, Npad, hd, scale, causal, st)) != FA_OK) return s;
+  if ((s = run_kv<KV7>(q, k, v, dO, w, dk, dv, BH, N, Npad, hd, scale, causal, qsplit, st)) != FA_OK) return s;
   return run_q<Q7>(q, k, v, dO, w, dq, BH, N, Npad, hd, scale, causal, st);
 }
 
@@ -196,6 +222,92 @@ bool bwd_supported(int d, int variant) {
   return false;
 }
 
-int bwd_launch_count(int, int) { return 3; }
+int bwd_launch_count(int BH, int N, int d, int causal, int variant) {
+  return 3 + (choose_qsplit(BH, N, d, causal, variant) > 1 ? 1 : 0);
+}
+
+size_t bwd_split_bytes(int BH, int N, int d, int causal, int variant) {
+  const int qsplit = choose_qsplit(BH, N, d, causal, variant);
+  if (qsplit <= 1) return 0;
+  const size_t npad = (size_t)(N + 127) / 128 * 128;
+  return 2 * 4 * (size_t)qsplit * BH * npad * (size_t)padded_head_dim(d);
+}
+
+// Query parts per key tile for the dK/dV kernel.  A persistent grid finishes no
+// earlier than its longest work item; with few heads there are fewer key tiles
+// than SMs, and under the causal mask the first key tile of a head sees every
+// query tile, so splitting the query range shortens the critical path at the
+// price of more item changes and a summing kernel.  The model replays the
+// kernel's dynamic claiming (items in launch order, each taken by the SM that
+// frees first) with per-query-tile and per-item costs in SM cycles, adds the
+// summing kernel's traffic, and keeps the cheapest part count.
+namespace {
+int choose_qsplit_uncached(int BH, int N, int d, int causal, int variant);
+std::mutex g_qsplit_mutex;
+std::map<std::tuple<int, int, int, int, int, int>, int> g_qsplit_cache;
+}  // namespace
+
+int choose_qsplit(int BH, int N, int d, int causal, int variant) {
+  const auto key = std::make_tuple(BH, N, d, causal, variant, sm_count_cached());
+  {
+    std::lock_guard<std::mutex> lock(g_qsplit_mutex);
+    auto it = g_qsplit_cache.find(key);
+    if (it != g_qsplit_cache.end()) return it->second;
+  }
+  const int q = choose_qsplit_uncached(BH, N, d, causal, variant);
+  std::lock_guard<std::mutex> lock(g_qsplit_mutex);
+  if (g_qsplit_cache.size() > 4096) g_qsplit_cache.clear();
+  g_qsplit_cache[key] = q;
+  return q;
+}
+
+namespace {
+int choose_qsplit_uncached(int BH, int N, int d, int causal, int variant) {
+  const int D = padded_head_dim(d);
+  if (D == 0 || BH <= 0 || N <= 0) return 1;
+  const bool five = variant == FA_BWD_5GEMM;
+  const int bm = D == 64 ? 128 : 64;                 // query rows per step
+  const int dsplit = (!five && D == 256) ? 2 : 1;    // d = 192 / 256: dV and dK items
+  const int n_kt = (N + 127) / 128, n_qt = (N + bm - 1) / bm;
+  const double sms = sm_count_cached();
+  if ((double)n_kt * dsplit * BH >= 2.0 * sms) return 1;
+  const double gemms = five ? 5.0 : (D == 256 ? 2.5 : 4.0);  // per item and query step
+  const double step = gemms * 2.0 * 128.0 * bm * d / (8192.0 * 0.55);  // cycles
+  const double item_cycles = 7000.0;
+  const double cycles_per_us = 1900.0;
+  double best_us = 0.0;
+  int best = 1;
+  const int max_parts = std::min(16, n_qt);
+  for (int parts = 1; parts <= max_parts; ++parts) {
+    // Min-heap of the SMs' next free times.
+    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+    for (int i = 0; i < (int)sms; ++i) free_at.push(0.0);
+    double makespan = 0.0;
+    // Launch order: key tiles first to last (under the causal mask the first is the
+    // heaviest), then parts, d parts and heads.
+    for (int kt = 0; kt < n_kt; ++kt) {
+      const int first = causal ? (kt * 128) / bm : 0;
+      const int total = n_qt - first;
+      for (int s = 0; s < parts; ++s) {
+        const int n = (int)((long long)(s + 1) * total / parts) - (int)((long long)s * total / parts);
+        const double c = n * step + item_cycles;
+        for (int h = 0; h < dsplit * BH; ++h) {
+          const double t = free_at.top() + c;
+          free_at.pop();
+          free_at.push(t);
+          makespan = std::max(makespan, t);
+        }
+      }
+    }
+    double us = makespan / cycles_per_us;
+    if (parts > 1) us += 4.0 + (double)BH * N * (2.0 * 4 * parts * D + 4.0 * d) / 6.0e6;
+    if (parts == 1 || us < 0.97 * best_us) {
+      best = parts;
+      best_us = us;
+    }
+  }
+  return best;
+}
+}  // namespace
 
 }  // namespace fa

@@ -179,9 +179,58 @@ struct BwdKVParams {
   float scale;
   int causal;
   int group;  // heads per launch-order group
-  int items;  // work items (key tiles x d parts x heads); the grid is persistent over them
+  int items;  // work items (key tiles x query parts x d parts x heads); the grid is persistent over them
   int* sched; // next unclaimed work item (zero at launch)
+  // Query-range split (few heads, long sequences): each key tile's query tiles are
+  // cut into `qsplit` contiguous parts, each a work item of its own.  With
+  // qsplit > 1 an item writes its fp32 dK and dV sums over its part (dK without
+  // the scale) to dkpart / dvpart [qsplit][BH][Npad][D] instead of dk / dv, and
+  // bwd_kvsum_kernel adds the parts.
+  int qsplit;
+  float* dkpart;
+  float* dvpart;
 };
+
+// Sum of the query-range parts of dK and dV: dV = sum_s dvpart[s], dK = scale *
+// sum_s dkpart[s] (parts in fixed order, so the result is reproducible), bf16.
+struct KVSumParams {
+  const float* dkpart;
+  const float* dvpart;
+  uint16_t* dk;
+  uint16_t* dv;
+  int* err;
+  int N, Npad, BH, hd, D, parts;
+  float scale;
+};
+
+static __global__ void __launch_bounds__(256) bwd_kvsum_kernel(const KVSumParams p) {
+  grid_dep_wait();
+  if (*reinterpret_cast<volatile const int*>(p.err) != 0) return;
+  const int tpr = p.hd / 8;
+  const long long g = (long long)blockIdx.x * 256 + threadIdx.x;
+  const long long row = g / tpr;  // bh * N + j
+  if (row >= (long long)p.BH * p.N) return;
+  const int c = (int)(g - row * tpr) * 8;
+  const int bh = (int)(row / p.N), j = (int)(row % p.N);
+  const size_t off = ((size_t)bh * p.Npad + j) * p.D + c;
+  const size_t stride = (size_t)p.BH * p.Npad * p.D;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, b[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < p.parts; ++s) {
+    const float4* v4 = reinterpret_cast<const float4*>(p.dvpart + s * stride + off);
+    const float4* k4 = reinterpret_cast<const float4*>(p.dkpart + s * stride + off);
+    const float4 v0 = v4[0], v1 = v4[1], k0 = k4[0], k1 = k4[1];
+    a[0] += v0.x; a[1] += v0.y; a[2] += v0.z; a[3] += v0.w;
+    a[4] += v1.x; a[5] += v1.y; a[6] += v1.z; a[7] += v1.w;
+    b[0] += k0.x; b[1] += k0.y; b[2] += k0.z; b[3] += k0.w;
+    b[4] += k1.x; b[5] += k1.y; b[6] += k1.z; b[7] += k1.w;
+  }
+  const float sc = p.scale;
+  *reinterpret_cast<uint4*>(p.dv + (size_t)row * p.hd + c) =
+      make_uint4(pack_bf16(a[0], a[1]), pack_bf16(a[2], a[3]), pack_bf16(a[4], a[5]), pack_bf16(a[6], a[7]));
+  *reinterpret_cast<uint4*>(p.dk + (size_t)row * p.hd + c) =
+      make_uint4(pack_bf16(b[0] * sc, b[1] * sc), pack_bf16(b[2] * sc, b[3] * sc), pack_bf16(b[4] * sc, b[5] * sc),
+                 pack_bf16(b[6] * sc, b[7] * sc));
+}
 
 template <int D_, int BM_, bool DQ_, int DSPLIT_, int QS_, bool SEP_, bool VT_ = false, bool OS_ = false>
 struct BwdKVCfg {
@@ -347,16 +396,23 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
     return w;
   };
   struct Item {
-    int bh, h, k0, qt0, n;  // head, d part, first key, first query tile, query tiles
+    int bh, h, part, k0, qt0, n;  // head, d part, query part, first key, first query tile, query tiles
   };
+  // Item w: key tile, query part and d part from the launch order; the key tile's
+  // query tiles (from the diagonal under the causal mask) are cut into p.qsplit
+  // contiguous parts (some possibly empty when there are fewer tiles than parts).
   auto coords = [&](int w) {
     Item I;
     int tile;
-    grouped_order(w, n_kt * C::DSPLIT, p.BH, p.group, tile, I.bh);
+    grouped_order(w, n_kt * C::DSPLIT * p.qsplit, p.BH, p.group, tile, I.bh);
     I.h = tile % C::DSPLIT;
-    I.k0 = (tile / C::DSPLIT) * C::BN;
-    I.qt0 = p.causal ? I.k0 / BM : 0;
-    I.n = n_qt - I.qt0;
+    const int kq = tile / C::DSPLIT;
+    I.part = kq % p.qsplit;
+    I.k0 = (kq / p.qsplit) * C::BN;
+    const int first = p.causal ? I.k0 / BM : 0;
+    const int total = n_qt - first;
+    I.qt0 = first + (int)((long long)I.part * total / p.qsplit);
+    I.n = first + (int)((long long)(I.part + 1) * total / p.qsplit) - I.qt0;
     return I;
   };
 
@@ -674,8 +730,19 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         const int kj = I.k0 + r;
         const bool key_ok = kj < p.N;
         if (I.n <= 0) {
-          // No query can see this key tile: zero gradients.
+          // No query of this item can see the key tile: zero gradients (zero partial
+          // sums under the query-range split).
           const int c_off = C::OS ? 0 : I.h * DH;
+          if (p.qsplit > 1) {
+            if (key_ok && cw == 0) {
+              const size_t off = (((size_t)I.part * p.BH + I.bh) * p.Npad + kj) * D + c_off;
+              for (int c = 0; c < DH; c += 4) {
+                if (!C::OS || I.h == 0) *reinterpret_cast<float4*>(p.dvpart + off + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (!C::OS || I.h == 1) *reinterpret_cast<float4*>(p.dkpart + off + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+              }
+            }
+            continue;
+          }
           if (key_ok && cw == 0)
             for (int c = 0; c < DH; c += 8) {
               if (c_off + c < p.hd) {
@@ -824,6 +891,33 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         // item's first query tile, whose dV / dK MMAs overwrite the accumulators.
         if (!wait_warp(BAR(C::B_MMA), (g - 1) & 1, ab, (kKBwdKV << 8) | 10)) break;
         tc_fence_after();
+        if (p.qsplit > 1) {
+          // Query-range split: this part's fp32 sums (dK without the scale), one row per thread.
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            if (C::NCW == 2 && which != cw) continue;
+            if (C::OS && which != I.h) continue;
+            const int c_off = C::OS ? 0 : I.h * DH;
+            float* dst = (which == 0 ? p.dvpart : p.dkpart) + (((size_t)I.part * p.BH + I.bh) * p.Npad + kj) * D + c_off;
+            const uint32_t tacc = trow + (which == 0 ? C::T_DV : C::T_DK);
+#pragma unroll
+            for (int c0 = 0; c0 < DH; c0 += 32) {
+              uint32_t rv[32];
+              tmem_ld_32x32b_x32(tacc + c0, rv);
+              tmem_wait_ld();
+              reg_fence<32>(rv);
+              if (key_ok) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                  *reinterpret_cast<float4*>(dst + c0 + e) =
+                      make_float4(__uint_as_float(rv[e]), __uint_as_float(rv[e + 1]), __uint_as_float(rv[e + 2]),
+                                  __uint_as_float(rv[e + 3]));
+              }
+            }
+          }
+          tc_fence_before();
+          continue;
+        }
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           if (C::NCW == 2 && which != cw) continue;  // two warpgroups: one stores dV, the other dK

@@ -110,6 +110,9 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   kp.group = causal ? l2_head_group(12.0 * N * D, BH, ((N + KV::BN - 1) / KV::BN) * KV::DSPLIT)
                     : head_group(((N + KV::BN - 1) / KV::BN) * KV::DSPLIT, BH);
   kp.sched = sched;
+  kp.qsplit = 1;  // no query-range split: its partial sums would need more scratch
+  kp.dkpart = nullptr;
+  kp.dvpart = nullptr;
   const long long kv_items = (long long)((N + KV::BN - 1) / KV::BN) * BH * KV::DSPLIT;
   if (kv_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   kp.items = (int)kv_items;

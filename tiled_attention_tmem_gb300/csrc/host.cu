@@ -213,10 +213,19 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, int variant) {
   if (variant != FA_BWD_AUTO && variant != FA_BWD_5GEMM && variant != FA_BWD_7GEMM) return 0;
   const size_t bh = (size_t)B * H;
   const size_t npad = round_up((size_t)N, 128);
-  size_t bytes = 2 * round_up(4 * bh * npad, 256);  // log2-domain LSE and D per padded row
-  if (variant != FA_BWD_7GEMM && bwd_supported(d, FA_BWD_5GEMM))
-    bytes += 4 * bh * npad * (size_t)padded_head_dim(d);  // fp32 dQ accumulator (padded head dim)
-  return bytes + 256;
+  size_t rows = 2 * round_up(4 * bh * npad, 256);  // log2-domain LSE and D per padded row
+  // The variant's own needs: the 5-GEMM fp32 dQ accumulator (padded head dim) and
+  // the partial dK / dV of the dK/dV kernel's query-range split.
+  size_t five = 0, seven = 0;
+  if (bwd_supported(d, FA_BWD_5GEMM))
+    five = 4 * bh * npad * (size_t)padded_head_dim(d) + bwd_split_bytes(B * H, N, d, 1, FA_BWD_5GEMM);
+  seven = bwd_split_bytes(B * H, N, d, 1, FA_BWD_7GEMM);
+  // The split count depends on the mask; size for the larger of the two.
+  if (bwd_supported(d, FA_BWD_5GEMM))
+    five = std::max(five, 4 * bh * npad * (size_t)padded_head_dim(d) + bwd_split_bytes(B * H, N, d, 0, FA_BWD_5GEMM));
+  seven = std::max(seven, bwd_split_bytes(B * H, N, d, 0, FA_BWD_7GEMM));
+  const size_t extra = variant == FA_BWD_5GEMM ? five : variant == FA_BWD_7GEMM ? seven : std::max(five, seven);
+  return rows + extra + 256;
 }
 
 // Measured on GB300 over the sequence sweep (N = 512..16384, both masks) and
@@ -328,6 +337,7 @@ const char* fa_kernel_name(int kind) {
     case FA_KERNEL_BWD_KV7: return "bwd_kv7";
     case FA_KERNEL_BWD_Q7: return "bwd_q7";
     case FA_KERNEL_FWD_MERGE: return "fwd_merge";
+    case FA_KERNEL_BWD_KVSUM: return "bwd_kvsum";
   }
   return "unknown";
 }
@@ -346,7 +356,7 @@ int fa_bwd_launches(int B, int H, int N, int d, int variant, int causal) {
   if ((long long)B * H * N <= 0 || !supported_d(d)) return 0;
   const int v = variant == FA_BWD_AUTO ? fa_bwd_choose(B, H, N, d, causal) : variant;
   if (!bwd_supported(d, v)) return 0;
-  return bwd_launch_count(d, v);
+  return bwd_launch_count(B * H, N, d, causal, v);
 }
 
 }  // extern "C"

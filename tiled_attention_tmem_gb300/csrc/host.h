@@ -97,6 +97,10 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
                   const float* lse, void* dq, void* dk, void* dv, int BH, int N, int d,
                   float scale, int causal, int variant, void* workspace, cudaStream_t st);
 bool bwd_supported(int d, int variant);
-int bwd_launch_count(int d, int variant);
+int bwd_launch_count(int BH, int N, int d, int causal, int variant);
+// Query parts per key tile of the dK/dV kernel (1: no split) and the workspace
+// bytes of its fp32 partial dK / dV (0 without a split).
+int choose_qsplit(int BH, int N, int d, int causal, int variant);
+size_t bwd_split_bytes(int BH, int N, int d, int causal, int variant);
 
 }  // namespace fa
