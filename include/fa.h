@@ -66,8 +66,10 @@ typedef enum {
 
 /*
  * Forward.  q, k, v: [B,H,N,d] bf16 (read).  o: [B,H,N,d] bf16 (written).
- * lse: [B,H,N] fp32 (written), natural log.  d must be 64, 96, 128, 192 or 256
- * (96 runs the 128 kernels on zero-padded tiles; 192 has its own).
+ * lse: [B,H,N] fp32 (written), natural log.  d must be 64, 96, 128, 192, 256 or
+ * 384 (96 runs the 128 kernels on zero-padded tiles; 192 and 384 have their own;
+ * at 384 the backward is the 7-GEMM form with lopsided tiles: dV and dK in three
+ * column parts per key tile and 32 queries per step, dQ in two column parts).
  * scale: finite and > 0 (typically 1/sqrt(d)).  causal: 0 or 1 (key j is
  * visible to query i iff j <= i).  B*H*N == 0 is a no-op returning FA_OK.
  */

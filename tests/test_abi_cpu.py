@@ -207,6 +207,8 @@ def test_bwd_noalloc_validation(lib):
     # head dims above 128 have no 5-GEMM kernel
     assert call(d=256, variant=b.FA_BWD_5GEMM) == b.FA_ERR_UNSUPPORTED
     assert call(d=192, variant=b.FA_BWD_5GEMM) == b.FA_ERR_UNSUPPORTED
+    assert call(d=384, variant=b.FA_BWD_5GEMM) == b.FA_ERR_UNSUPPORTED
+    assert call(d=320) == b.FA_ERR_UNSUPPORTED
     # scratch beyond the static array is refused before anything is launched
     big = dict(B=64, H=64, N=8192)
     assert call(d=128, variant=b.FA_BWD_7GEMM, **big) == b.FA_ERR_WORKSPACE

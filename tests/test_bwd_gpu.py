@@ -33,8 +33,17 @@ SMALL = [
     (1, 2, 17, 192, True, 1.0, 0.0, None),
     (1, 1, 1, 256, False, 1.0, 0.0, None),
     (2, 1, 65, 256, True, 0.5, 0.0, 1.0 / 16),
+    # head dim 384 (dV and dK in three column parts, dQ in two), both masks
+    (1, 1, 1, 384, False, 1.0, 0.0, None),
+    (1, 2, 1, 384, True, 1.0, 0.0, None),
+    (1, 1, 129, 384, False, 1.0, 0.0, None),
+    (1, 2, 129, 384, True, 1.0, 0.0, None),
+    (1, 1, 1024, 384, False, 1.0, 0.0, None),
+    (1, 1, 1024, 384, True, 1.0, 0.0, None),
+    (2, 1, 333, 384, True, 0.5, 3.0, 1.0 / 20),
     # more work items than SMs: each persistent CTA claims several, short ones among them
     (2, 96, 256, 256, True, 0.5, 0.0, 1.0 / 16),
+    (1, 160, 130, 384, True, 0.5, 0.0, None),
     (1, 200, 256, 128, True, 1.0, 0.0, None),
 ]
 
@@ -94,6 +103,14 @@ def test_seven_gemm_is_bitwise_reproducible():
     x = I.make_inputs(2, 2, 640, 128, seed=9)
     a = _fwd_bwd(x, 2, 2, 640, 128, 0.0884, True, V7)
     b = _fwd_bwd(x, 2, 2, 640, 128, 0.0884, True, V7)
+    for u, w in zip(a, b):
+        assert np.array_equal(to_f64(u), to_f64(w))
+
+
+def test_seven_gemm_is_bitwise_reproducible_at_d384():
+    x = I.make_inputs(1, 2, 700, 384, seed=19)
+    a = _fwd_bwd(x, 1, 2, 700, 384, 384 ** -0.5, True, V7)
+    b = _fwd_bwd(x, 1, 2, 700, 384, 384 ** -0.5, True, V7)
     for u, w in zip(a, b):
         assert np.array_equal(to_f64(u), to_f64(w))
 

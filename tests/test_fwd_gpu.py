@@ -35,9 +35,19 @@ SMALL = [
     (1, 2, 17, 192, True, 1.0, 0.0, None),
     (1, 1, 1, 256, False, 1.0, 0.0, None),
     (2, 1, 65, 256, True, 0.5, 0.0, 1.0 / 16),
+    # head dim 384 (Q in shared memory, S double-buffered next to a 384-column O):
+    # one row, ragged tails, several tiles, both masks
+    (1, 1, 1, 384, False, 1.0, 0.0, None),
+    (1, 2, 1, 384, True, 1.0, 0.0, None),
+    (1, 1, 129, 384, False, 1.0, 0.0, None),
+    (1, 2, 129, 384, True, 1.0, 0.0, None),
+    (1, 1, 1024, 384, False, 1.0, 0.0, None),
+    (1, 1, 1024, 384, True, 1.0, 0.0, None),
+    (2, 1, 333, 384, True, 0.5, 3.0, 1.0 / 20),
     # more work items than SMs, so that each persistent CTA runs several items,
     # short ones (one or two key tiles) among them
     (2, 96, 256, 256, True, 0.5, 0.0, 1.0 / 16),
+    (1, 160, 130, 384, True, 0.5, 0.0, None),
     (1, 200, 256, 128, True, 1.0, 0.0, None),
     (1, 200, 130, 64, True, 1.0, 0.0, None),
 ]

@@ -35,6 +35,7 @@ CASES = [
     # a single row: one key tile, the second part empty
     (1, 1, 1, 64, False, 2, 1.0, None),
     (2, 1, 640, 256, False, 7, 1.0, None),
+    (1, 1, 700, 384, True, 3, 1.0, None),
     (1, 1, 2048, 128, True, 16, 1.0, None),
     (1, 1, 4096, 64, False, 64, 1.0, None),
     # a large shift of the key means: partial maxima far apart across parts

@@ -33,7 +33,14 @@ def _shapes():
     return out
 
 
-SHAPES = _shapes()
+def _shapes_384():
+    """Three more draws at head dim 384 (a seed of their own, so the set above stays)."""
+    rng = np.random.default_rng(20261204)
+    return [(int(rng.integers(1, 3)), int(rng.integers(1, 3)), int(rng.integers(1, 701)), 384,
+             bool(rng.integers(0, 2)), float(rng.uniform(0.02, 0.1)), 3100 + k) for k in range(3)]
+
+
+SHAPES = _shapes() + _shapes_384()
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "b{}h{}n{}d{}{}".format(*s[:4], "c" if s[4] else ""))

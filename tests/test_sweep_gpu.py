@@ -3,8 +3,8 @@ the bench measures (fa_fwd, then fa_bwd with every variant the head dim has, on
 the whole [B, H, N, d] problem), checked against the fp64 CPU oracle.
 
 Sequence sweep: all 24 points (B*N = 16384 tokens, H = 16, N from 512 to 16384,
-d in {64, 128}, both masks).  Head-dim sweep: all 10 points (B = 4, H = 16,
-N = 4096, d in {64, 96, 128, 192, 256}, both masks).
+d in {64, 128}, both masks).  Head-dim sweep: all 12 points (B = 4, H = 16,
+N = 4096, d in {64, 96, 128, 192, 256, 384}, both masks).
 
 At each point, on sampled heads (the first, the last and one in the middle):
 the forward on sampled rows (computed row by row by the oracle), and the

@@ -32,6 +32,7 @@ CASES = [
     # head dims run on zero-padded tiles
     (1, 2, 300, 96, True, b.FA_BWD_5GEMM),
     (1, 2, 200, 192, False, b.FA_BWD_AUTO),
+    (1, 2, 300, 384, True, b.FA_BWD_AUTO),
 ]
 
 

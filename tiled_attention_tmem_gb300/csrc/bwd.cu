@@ -28,11 +28,18 @@ using KV7_192 = BwdKVCfg<192, 64, false, 1, 2, false>;
 // d = 256: V in TMEM, and the outputs split (a dV item and a dK item per key tile, each with one
 // 256-column accumulator).
 using KV7_256 = BwdKVCfg<256, 64, false, 2, 2, false, true, true>;
+// d = 384: dV and dK cut into three column parts of 128, one work item each (every item
+// recomputes S^T and dP^T), 32 queries per step, V in TMEM: 32 + 32 + 128 + 128 + 192 = 512
+// TMEM columns next to a 96 KiB K tile and two 48 KiB query stages.
+using KV7_384 = BwdKVCfg<384, 32, false, 3, 2, false, true, false>;
 // dQ kernel configurations <d, keys per tile, K/V ring slots>.
 using Q7_64 = BwdQCfg<64, 128, 6>;
 using Q7_128 = BwdQCfg<128, 128, 4>;
 using Q7_192 = BwdQCfg<192, 64, 7, true>;
 using Q7_256 = BwdQCfg<256, 64, 5, true>;
+// d = 384: two dQ column parts of 192 per query tile (one work item each), dO in TMEM,
+// 32-key tiles, four K/V slots of 24 KiB next to the 96 KiB Q tile.
+using Q7_384 = BwdQCfg<384, 32, 4, true, 2>;
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -126,9 +133,11 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
   p.items = (int)items;
   // Persistent grid: one CTA per SM (one fits per SM), each walking its items.
   const long long grid = std::min<long long>(items, sm_count_cached());
-  fa_status s2 = launch(C::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<C>, dim3((unsigned)grid),
-                        dim3(C::THREADS), C::SMEM_BYTES, st, p);
-  if (s2 != FA_OK || qsplit <= 1) return s2;
+  const int kind = C::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7;
+  if (qsplit <= 1)
+    return launch(kind, bwd_kv_kernel<C, false>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  fa_status s2 = launch(kind, bwd_kv_kernel<C, true>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  if (s2 != FA_OK) return s2;
   KVSumParams sp{w.dkpart, w.dvpart, static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv), p.err,
                  N, Npad, BH, hd, C::D, qsplit, scale};
   const long long threads = (long long)BH * N * (hd / 8);
@@ -159,9 +168,10 @@ fa_status run_q(const void* q, const void* k, const void* v, const void* dO, con
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
-  p.group = causal ? l2_head_group(12.0 * N * C::D, BH, (N + 127) / 128) : head_group((N + 127) / 128, BH);
+  const int tiles = ((N + 127) / 128) * C::DQS;
+  p.group = causal ? l2_head_group(12.0 * N * C::D, BH, tiles) : head_group(tiles, BH);
   p.sched = w.sched;
-  const long long items = (long long)((N + 127) / 128) * BH;
+  const long long items = (long long)tiles * BH;
   if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.items = (int)items;
   // Persistent grid: one CTA per SM, each claiming work items.
@@ -200,6 +210,9 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
                   void* workspace, cudaStream_t st) {
   if (d == 192)
     return run_d<256, void, KV7_192, Q7_192>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, variant,
+                                             workspace, st);
+  if (d == 384)
+    return run_d<384, void, KV7_384, Q7_384>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, variant,
                                              workspace, st);
   switch (padded_head_dim(d)) {
     case 64:
@@ -266,12 +279,14 @@ int choose_qsplit_uncached(int BH, int N, int d, int causal, int variant) {
   const int D = padded_head_dim(d);
   if (D == 0 || BH <= 0 || N <= 0) return 1;
   const bool five = variant == FA_BWD_5GEMM;
-  const int bm = D == 64 ? 128 : 64;                 // query rows per step
-  const int dsplit = (!five && D == 256) ? 2 : 1;    // d = 192 / 256: dV and dK items
+  const int bm = D == 64 ? 128 : D == 384 ? 32 : 64;  // query rows per step
+  // d = 256: a dV item and a dK item per key tile; d = 384: three column parts.
+  const int dsplit = (!five && D == 256) ? 2 : D == 384 ? 3 : 1;
   const int n_kt = (N + 127) / 128, n_qt = (N + bm - 1) / bm;
   const double sms = sm_count_cached();
   if ((double)n_kt * dsplit * BH >= 2.0 * sms) return 1;
-  const double gemms = five ? 5.0 : (D == 256 ? 2.5 : 4.0);  // per item and query step
+  // GEMMs of 2 * 128 * bm * d FLOPs per item and query step
+  const double gemms = five ? 5.0 : (D == 256 ? 2.5 : D == 384 ? 2.0 + 2.0 / 3.0 : 4.0);
   const double step = gemms * 2.0 * 128.0 * bm * d / (8192.0 * 0.55);  // cycles
   const double item_cycles = 7000.0;
   const double cycles_per_us = 1900.0;

@@ -45,7 +45,8 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // ----------------------------------------------------------------- preprocess
-// One group of G = d/8 threads per row: D_i = sum_c dO_ic O_ic (fp32), the
+// One group of G threads per row (G = d/8 up to 32, 16 at d = 384), each
+// taking CH chunks of 8 columns: D_i = sum_c dO_ic O_ic (fp32), the
 // log2-domain LSE (both stored negated), and (5-GEMM) zeroing of the row's fp32
 // dQ accumulator.
 struct PreParams {
@@ -62,7 +63,9 @@ struct PreParams {
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
   grid_dep_wait();
-  constexpr int G = D / 8;
+  constexpr int G = D / 8 <= 32 ? D / 8 : 16;  // threads per row (a power of two)
+  constexpr int CH = D / 8 / G;                // 8-column chunks per thread
+  static_assert(G * CH * 8 == D && (G & (G - 1)) == 0, "preprocess row split");
   const long long rows = (long long)p.BH * p.Npad;
   const int sub = threadIdx.x % G;
   for (long long row = ((long long)blockIdx.x * 256 + threadIdx.x) / G; row < rows;
@@ -70,15 +73,19 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
     const int bh = (int)(row / p.Npad);
     const int i = (int)(row % p.Npad);
     float acc = 0.f;
-    if (i < p.N && sub * 8 < p.dv) {
-      const size_t off = ((size_t)bh * p.N + i) * p.dv + sub * 8;
-      const uint4 a = *reinterpret_cast<const uint4*>(p.o + off);
-      const uint4 b = *reinterpret_cast<const uint4*>(p.dO + off);
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        acc = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), acc);
-        acc = fmaf(__uint_as_float(av[e] & 0xffff0000u), __uint_as_float(bv[e] & 0xffff0000u), acc);
+    for (int ch = 0; ch < CH; ++ch) {
+      const int c = (ch * G + sub) * 8;
+      if (i < p.N && c < p.dv) {
+        const size_t off = ((size_t)bh * p.N + i) * p.dv + c;
+        const uint4 a = *reinterpret_cast<const uint4*>(p.o + off);
+        const uint4 b = *reinterpret_cast<const uint4*>(p.dO + off);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), acc);
+          acc = fmaf(__uint_as_float(av[e] & 0xffff0000u), __uint_as_float(bv[e] & 0xffff0000u), acc);
+        }
       }
     }
 #pragma unroll
@@ -89,9 +96,12 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const PreParams p) {
     }
     if (p.sched && row == 0 && sub < 4) p.sched[sub] = 0;
     if (p.dqacc) {
-      float4* z = reinterpret_cast<float4*>(p.dqacc + (size_t)row * D + sub * 8);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int ch = 0; ch < CH; ++ch) {
+        float4* z = reinterpret_cast<float4*>(p.dqacc + (size_t)row * D + (ch * G + sub) * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
     }
   }
 }
@@ -312,7 +322,9 @@ struct BwdKVCfg {
   static_assert(!OS || (VT && !DQ && !SEP && DSPLIT == 2), "output split: dV item and dK item per key tile");
 };
 
-template <class C>
+// QSPLIT: the query-range split instantiation (p.qsplit > 1); the plain one
+// keeps one part per key tile as a constant and has no partial-sum epilogue.
+template <class C, bool QSPLIT>
 __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_constant__ BwdKVParams p) {
   constexpr int D = C::D, BM = C::BM, QS = C::QS, DH = C::DH;
   extern __shared__ uint8_t smem_raw[];
@@ -397,23 +409,42 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
   };
   struct Item {
     int bh, h, part, k0, qt0, n;  // head, d part, query part, first key, first query tile, query tiles
+    int rot;                      // the item's first step takes query tile qt0 + rot (see qt_at)
   };
   // Item w: key tile, query part and d part from the launch order; the key tile's
   // query tiles (from the diagonal under the causal mask) are cut into p.qsplit
   // contiguous parts (some possibly empty when there are fewer tiles than parts).
+  const int qsplit = QSPLIT ? p.qsplit : 1;
   auto coords = [&](int w) {
     Item I;
     int tile;
-    grouped_order(w, n_kt * C::DSPLIT * p.qsplit, p.BH, p.group, tile, I.bh);
+    grouped_order(w, n_kt * C::DSPLIT * qsplit, p.BH, p.group, tile, I.bh);
     I.h = tile % C::DSPLIT;
     const int kq = tile / C::DSPLIT;
-    I.part = kq % p.qsplit;
-    I.k0 = (kq / p.qsplit) * C::BN;
-    const int first = p.causal ? I.k0 / BM : 0;
-    const int total = n_qt - first;
-    I.qt0 = first + (int)((long long)I.part * total / p.qsplit);
-    I.n = first + (int)((long long)(I.part + 1) * total / p.qsplit) - I.qt0;
+    if constexpr (QSPLIT) {
+      I.part = kq % qsplit;
+      I.k0 = (kq / qsplit) * C::BN;
+      const int first = p.causal ? I.k0 / BM : 0;
+      const int total = n_qt - first;
+      I.qt0 = first + (int)((long long)I.part * total / qsplit);
+      I.n = first + (int)((long long)(I.part + 1) * total / qsplit) - I.qt0;
+    } else {
+      I.part = 0;
+      I.k0 = kq * C::BN;
+      I.qt0 = p.causal ? I.k0 / BM : 0;
+      I.n = n_qt - I.qt0;
+    }
+    // Items of one head that run at the same time would otherwise walk the same
+    // query tiles in step (all of them from the first tile without the mask) and
+    // reduce into the same dQ rows at once; each key tile starts its walk at its
+    // own offset (n * kt / n_kt) and wraps around.
+    I.rot = I.n > 0 ? (int)((long long)I.n * (I.k0 / C::BN) / n_kt) : 0;
     return I;
+  };
+  // Query tile of step i of item I.
+  auto qt_at = [](const Item& I, int i) {
+    const int j = i + I.rot;
+    return I.qt0 + (j >= I.n ? j - I.n : j);
   };
 
   auto stage_q = [&](int s) { return sbase + C::OFF_STAGE + s * C::STAGE_BYTES; };
@@ -441,7 +472,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         int it = 0, nkv = 0;
         bool ok = true;
         auto prefetch_qd = [&](const Item& I, int i) {
-          const int prow = (I.qt0 + i) * BM;
+          const int prow = qt_at(I, i) * BM;
           for (int pn = 0; pn < C::PANELS; ++pn) {
             tma_prefetch_l2_3d(&p.q_map, 64 * pn, prow, I.bh);
             tma_prefetch_l2_3d(&p.do_map, 64 * pn, prow, I.bh);
@@ -470,7 +501,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           auto issue_stage = [&](int i) -> bool {
             const int s = it % QS;
             if (!wait_one(BAR(C::B_QDEMPTY + s), ((it / QS) & 1) ^ 1, ab, (kKBwdKV << 8) | 1)) return false;
-            const int qrow = (I.qt0 + i) * BM;
+            const int qrow = qt_at(I, i) * BM;
             mbar_expect_tx(BAR(C::B_QDFULL + s), C::STAGE_TX);
             for (int pn = 0; pn < C::PANELS; ++pn) {
               tma_load_3d(stage_q(s) + pn * C::QD_PANEL, &p.q_map, BAR(C::B_QDFULL + s), 64 * pn, qrow, I.bh);
@@ -733,7 +764,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           // No query of this item can see the key tile: zero gradients (zero partial
           // sums under the query-range split).
           const int c_off = C::OS ? 0 : I.h * DH;
-          if (p.qsplit > 1) {
+          if constexpr (QSPLIT) {
             if (key_ok && cw == 0) {
               const size_t off = (((size_t)I.part * p.BH + I.bh) * p.Npad + kj) * D + c_off;
               for (int c = 0; c < DH; c += 4) {
@@ -781,7 +812,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         }
         for (int i = 0; i < I.n; ++i, ++g) {
           const int s = g % QS;
-          const int q0 = (I.qt0 + i) * BM;
+          const int q0 = qt_at(I, i) * BM;
           if (!wait_warp(BAR(C::B_SDP), g & 1, ab, (kKBwdKV << 8) | 7) ||
               !wait_warp(BAR(C::B_QDFULL + s), (g / QS) & 1, ab, (kKBwdKV << 8) | 8)) {
             ok = false;
@@ -891,7 +922,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         // item's first query tile, whose dV / dK MMAs overwrite the accumulators.
         if (!wait_warp(BAR(C::B_MMA), (g - 1) & 1, ab, (kKBwdKV << 8) | 10)) break;
         tc_fence_after();
-        if (p.qsplit > 1) {
+        if constexpr (QSPLIT) {
           // Query-range split: this part's fp32 sums (dK without the scale), one row per thread.
 #pragma unroll
           for (int which = 0; which < 2; ++which) {
@@ -1019,7 +1050,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(BAR(C::B_DQFREE));
-          const int q0 = (I.qt0 + i) * BM;
+          const int q0 = qt_at(I, i) * BM;
           // The previous bulk reduction must have finished reading the staging tile.
           if (leader) {
             bulk_wait_read0();
@@ -1101,9 +1132,13 @@ struct BwdQParams {
 // dP = dO V^T takes A from TMEM; the shared memory this saves holds more K/V
 // slots, and the MMA order becomes S(j+1) (once the compute warps hold S(j) in
 // registers), dQ(j), dP(j+1), so that S(j+1) runs during the softmax of j.
-template <int D_, int BN_, int STAGES_, bool DT_ = false>
+// DQS: the dQ columns are cut into DQS parts, each a work item of its own that
+// recomputes S, dP and dS for its query tile (head dim 384, where the whole dQ
+// accumulator does not fit TMEM next to S, dP and dO).
+template <int D_, int BN_, int STAGES_, bool DT_ = false, int DQS_ = 1>
 struct BwdQCfg {
-  static constexpr int D = D_, BN = BN_, STAGES = STAGES_;
+  static constexpr int D = D_, BN = BN_, STAGES = STAGES_, DQS = DQS_;
+  static constexpr int DQW = D / DQS;  // dQ columns per work item
   static constexpr bool DT = DT_;
   static constexpr int PANELS = D / 64;
   static constexpr uint32_t Q_PANEL = 128 * 128;
@@ -1124,12 +1159,13 @@ struct BwdQCfg {
   static constexpr uint32_t OFF_MISC = OFF_BAR + NBAR * 8;
   static constexpr uint32_t SMEM_BYTES = OFF_MISC + 32 + 1024;
   static constexpr int T_S = 0, T_DP = BN, T_DQ = 2 * BN;
-  static constexpr int T_DO = 2 * BN + D;  // DT: dO as packed bf16 pairs, D / 2 columns
-  static constexpr int TMEM_USED = 2 * BN + D + (DT ? D / 2 : 0);
+  static constexpr int T_DO = 2 * BN + DQW;  // DT: dO as packed bf16 pairs, D / 2 columns
+  static constexpr int TMEM_USED = 2 * BN + DQW + (DT ? D / 2 : 0);
   static constexpr uint32_t TMEM_COLS = TMEM_USED <= 256 ? 256 : 512;
   static constexpr int THREADS = 256;
   static_assert(TMEM_USED <= 512 && SMEM_BYTES <= 232448, "budgets");
   static_assert(!DT || BN <= 64, "DT holds a whole S and dP row of the tile in registers");
+  static_assert(DQW % 64 == 0 && DQW <= 256, "dQ MMA width: whole panels, N <= 256");
 };
 
 template <class C>
@@ -1188,12 +1224,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
   // across items.
   const int n_qt = (p.N + 127) / 128;
   struct Item {
-    int q0, bh, n;  // first query row, head, key tiles
+    int q0, bh, n, h;  // first query row, head, key tiles, dQ column part
   };
   auto coords = [&](int w) {
     Item I;
     int qt;
-    grouped_order(w, n_qt, p.BH, p.group, qt, I.bh);
+    grouped_order(w, n_qt * C::DQS, p.BH, p.group, qt, I.bh);
+    I.h = qt % C::DQS;
+    qt /= C::DQS;
     if (p.causal) qt = n_qt - 1 - qt;
     I.q0 = qt * 128;
     const int last = p.causal ? min(I.q0 + 127, p.N - 1) : p.N - 1;
@@ -1267,7 +1305,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
     } else if (warp == 1) {
       // Whole warp; one elected lane issues (see mma_ss).
       constexpr uint32_t idS = make_idesc(128, BN, false, false);
-      constexpr uint32_t idQ = make_idesc(128, D, false, true);
+      constexpr uint32_t idQ = make_idesc(128, C::DQW, false, true);
       bool ok = true;
       int it = 0, gj = 0, nitems = 0;
       if constexpr (C::DT) {
@@ -1330,9 +1368,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
               break;
             }
             tc_fence_after();
+            const uint32_t kq = kv_at(sk) + I.h * (C::DQW / 64) * C::KV_PANEL;  // this part's dQ columns of K
 #pragma unroll
             for (int k = 0; k < BN / 16; ++k)
-              mma_ts(tmem + C::T_DQ, tmem + C::T_DP + 8 * k, desc_mnmajor(kv_at(sk), C::KV_PANEL, 16 * k), idQ,
+              mma_ts(tmem + C::T_DQ, tmem + C::T_DP + 8 * k, desc_mnmajor(kq, C::KV_PANEL, 16 * k), idQ,
                      (j > 0 || k > 0) ? 1u : 0u);
             mma_commit(BAR(C::B_DQ));
             mma_commit(BAR(C::B_KVEMPTY + sk));
@@ -1381,9 +1420,10 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
             break;
           }
           tc_fence_after();
+          const uint32_t kq = kb + I.h * (C::DQW / 64) * C::KV_PANEL;  // this part's dQ columns of K
 #pragma unroll
           for (int k = 0; k < BN / 16; ++k)
-            mma_ts(tmem + C::T_DQ, tmem + C::T_DP + 8 * k, desc_mnmajor(kb, C::KV_PANEL, 16 * k), idQ,
+            mma_ts(tmem + C::T_DQ, tmem + C::T_DP + 8 * k, desc_mnmajor(kq, C::KV_PANEL, 16 * k), idQ,
                    (j > 0 || k > 0) ? 1u : 0u);
           mma_commit(BAR(C::B_DQ));
           mma_commit(BAR(C::B_KVEMPTY + sk));
@@ -1499,10 +1539,11 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
         if (!wait_warp(BAR(C::B_DQ), (gj - 1) & 1, ab, (kKBwdQ << 8) | 6)) break;
         tc_fence_after();
         const int row0 = I.q0 + quad * 32;
-        uint16_t* obase = p.dq + ((size_t)I.bh * p.N + (size_t)row0) * p.hd;
+        uint16_t* obase = p.dq + ((size_t)I.bh * p.N + (size_t)row0) * p.hd + I.h * C::DQW;
+        const int hd_left = p.hd - I.h * C::DQW;  // columns of this part inside the head dim
         uint8_t* epi = gbase + C::OFF_EPI + quad * 2048;
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < C::DQW; c0 += 32) {
           uint32_t rv[32];
           tmem_ld_32x32b_x32(trow + C::T_DQ + c0, rv);
           tmem_wait_ld();
@@ -1522,7 +1563,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
             for (int jj = 0; jj < 4; ++jj) {
               const int ri = jj * 8 + (lane >> 2), u = lane & 3;
               const uint4 val = *reinterpret_cast<const uint4*>(epi + ri * 64 + ((u ^ ((ri >> 1) & 3)) << 4));
-              if (row0 + ri < p.N && c0 + 8 * u < p.hd)
+              if (row0 + ri < p.N && c0 + 8 * u < hd_left)
                 *reinterpret_cast<uint4*>(obase + (size_t)ri * p.hd + c0 + 8 * u) = val;
             }
             __syncwarp();
@@ -1531,7 +1572,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
               uint4* o4 = reinterpret_cast<uint4*>(obase + (size_t)lane * p.hd + c0);
 #pragma unroll
               for (int v = 0; v < 4; ++v)
-                if (c0 + 8 * v < p.hd) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                if (c0 + 8 * v < hd_left) o4[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
             }
           }
         }

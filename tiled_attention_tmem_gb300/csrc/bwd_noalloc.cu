@@ -117,7 +117,7 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   if (kv_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   kp.items = (int)kv_items;
   const long long kv_grid = std::min<long long>(kv_items, sm_count_cached());
-  if ((s = launch(KV::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<KV>, dim3((unsigned)kv_grid),
+  if ((s = launch(KV::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7, bwd_kv_kernel<KV, false>, dim3((unsigned)kv_grid),
                   dim3(KV::THREADS), KV::SMEM_BYTES, st, kp)) != FA_OK)
     return s;
 
@@ -145,9 +145,10 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   qp.scale_log2 = scale * kLog2e;
   qp.scale = scale;
   qp.causal = causal;
-  qp.group = causal ? l2_head_group(12.0 * N * D, BH, (N + 127) / 128) : head_group((N + 127) / 128, BH);
+  const int q_tiles = ((N + 127) / 128) * Q7::DQS;
+  qp.group = causal ? l2_head_group(12.0 * N * D, BH, q_tiles) : head_group(q_tiles, BH);
   qp.sched = sched;
-  const long long q_items = (long long)((N + 127) / 128) * BH;
+  const long long q_items = (long long)q_tiles * BH;
   if (q_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   qp.items = (int)q_items;
   const long long q_grid = std::min<long long>(q_items, sm_count_cached());
@@ -166,6 +167,8 @@ using NQ7_64 = BwdQCfg<64, 128, 6>;
 using NQ7_128 = BwdQCfg<128, 128, 4>;
 using NQ7_192 = BwdQCfg<192, 64, 7, true>;
 using NQ7_256 = BwdQCfg<256, 64, 5, true>;
+using NKV7_384 = BwdKVCfg<384, 32, false, 3, 2, false, true, false>;
+using NQ7_384 = BwdQCfg<384, 32, 4, true, 2>;
 
 }  // namespace
 }  // namespace fa
@@ -191,7 +194,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
   // The variant fa_bwd would run; with AUTO, fall back to the 7-GEMM form when
   // only its smaller scratch fits.  Anything beyond the static array is refused.
   bool five = (variant == FA_BWD_AUTO ? fa_bwd_choose(B, H, N, d, causal) : variant) == FA_BWD_5GEMM;
-  if (five && D == 256) return FA_ERR_UNSUPPORTED;
+  if (five && D >= 256) return FA_ERR_UNSUPPORTED;
   if (five && scratch_need(BH, Npad, D, true) > kScratchBytes && variant == FA_BWD_AUTO) five = false;
   if (scratch_need(BH, Npad, D, five) > kScratchBytes) return FA_ERR_WORKSPACE;
   unsigned char* base = scratch_address();
@@ -206,6 +209,8 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
                                                 st)
                   : run<NKV7_128, NQ7_128, 128>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, false, base,
                                                 st);
+    case 384:
+      return run<NKV7_384, NQ7_384, 384>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, false, base, st);
     default:
       if (d == 192)
         return run<NKV7_192, NQ7_192, 256>(q, k, v, o, dO, lse, dq, dk, dv, BH, N, d, scale, causal, false, base, st);

@@ -12,6 +12,7 @@ namespace {
 //  d = 128: 2 x 128 query rows, 128 keys, 4 stages (Q 64 KiB + ring 128 KiB)
 //  d = 192: 1 x 128 query rows, 64 keys, 8 stages, Q in TMEM (ring 192 KiB)
 //  d = 256: 1 x 128 query rows, 64 keys, 6 stages, Q in TMEM (ring 192 KiB)
+//  d = 384: 1 x 128 query rows, 64 keys, 2 stages, Q in shared memory
 // d = 96 runs the d = 128 kernel: the TMA boxes read columns past d as zeros,
 // which leave S = QK^T unchanged and give zero output columns that are not
 // stored.
@@ -19,6 +20,10 @@ using Fwd64 = FwdCfg<64, 2, 128, 6>;
 using Fwd128 = FwdCfg<128, 2, 128, 4>;
 using Fwd192 = FwdCfg<192, 1, 64, 8, true>;
 using Fwd256 = FwdCfg<256, 1, 64, 6, true>;
+// d = 384: 1 x 128 query rows, 64 keys, Q in shared memory (96 KiB) with S
+// double-buffered in TMEM next to the 384-column O (512 columns), two K/V slots
+// of 48 KiB.
+using Fwd384 = FwdCfg<384, 1, 64, 2, false, true>;
 
 template <class C>
 fa_status run(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N, int d,
@@ -93,6 +98,7 @@ fa_status run_fwd(const void* q, const void* k, const void* v, void* o, float* l
     case 128: return run<Fwd128>(q, k, v, o, lse, BH, N, d, scale, causal, splits, workspace, st);
     case 192: return run<Fwd192>(q, k, v, o, lse, BH, N, d, scale, causal, splits, workspace, st);
     case 256: return run<Fwd256>(q, k, v, o, lse, BH, N, d, scale, causal, splits, workspace, st);
+    case 384: return run<Fwd384>(q, k, v, o, lse, BH, N, d, scale, causal, splits, workspace, st);
   }
   return FA_ERR_UNSUPPORTED;
 }

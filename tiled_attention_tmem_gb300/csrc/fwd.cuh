@@ -30,6 +30,11 @@
 // lets the softmax warps run from one key tile to the next without waiting for
 // S.  K/V tiles are loaded in that order (K one step ahead of V).
 //
+// QSD (d = 384): Q stays in shared memory (its 192 packed TMEM columns do not fit
+// next to the 384-column O), with the same double-buffered S and issue order as
+// QT; the producer loads each item's Q and the last S MMA of an item frees it.
+// O += P V runs as two MMAs of 192 columns (an MMA's N is at most 256).
+//
 // Split-KV (splits > 1): every query block becomes `splits` work items, item s
 // covering part s of the block's key tiles.  An item ends with O_s = O / l
 // normalised by its own sum (fp32) and its log2-domain log-sum-exp L_s = m + log2 l
@@ -75,11 +80,15 @@ struct FwdMergeParams {
   int splits;
 };
 
-template <int D_, int NQ_, int BN_, int STAGES_, bool QT_ = false>
+template <int D_, int NQ_, int BN_, int STAGES_, bool QT_ = false, bool QSD_ = false>
 struct FwdCfg {
   static constexpr int D = D_, NQ = NQ_, BN = BN_, STAGES = STAGES_;
-  static constexpr bool QT = QT_;
-  static constexpr int SB = QT ? 2 : 1;  // S buffers per query tile
+  static constexpr bool QT = QT_;    // Q in TMEM, S double-buffered
+  static constexpr bool QSD = QSD_;  // Q in shared memory, S double-buffered
+  static constexpr bool SD = QT || QSD;
+  static constexpr int SB = SD ? 2 : 1;  // S buffers per query tile
+  static constexpr int NPV = (D + 255) / 256;  // O += P V as NPV MMAs of PVN columns
+  static constexpr int PVN = D / NPV;
   static constexpr int BM = 128;
   static constexpr int PREFETCH = STAGES / 2 + 2;  // K/V tiles ahead for L2 prefetch
   static constexpr int PANELS = D / 64;
@@ -110,7 +119,8 @@ struct FwdCfg {
       TMEM_USED <= 32 ? 32 : TMEM_USED <= 64 ? 64 : TMEM_USED <= 128 ? 128 : TMEM_USED <= 256 ? 256 : 512;
   static constexpr int THREADS = 128 + 128 * NQ;
   static_assert(TMEM_USED <= 512, "TMEM budget");
-  static_assert(BN % 32 == 0 && BN <= 256 && D % 64 == 0 && D <= 256, "tile shape");
+  static_assert(BN % 32 == 0 && BN <= 256 && D % 64 == 0 && D <= 384 && PVN % 64 == 0, "tile shape");
+  static_assert(!(QT && QSD), "Q lives in one place");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
@@ -260,7 +270,17 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           if (w >= p.items) break;
           const Item I = coords(w);
           const Part P = part_of(w);
-          if constexpr (C::QT) {
+          if constexpr (C::SD) {
+            if (C::QSD && I.nmax > 0) {
+              // This item's Q, once the previous item's S MMAs are done reading Q.
+              if (!wait_one(BAR(C::B_QEMPTY), (nitems & 1) ^ 1, ab, (kKFwd << 8) | 10)) break;
+              mbar_expect_tx(BAR(C::B_QFULL), NQ * C::Q_TILE);
+              for (int t = 0; t < NQ; ++t)
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                  tma_load_3d(sbase + C::OFF_Q + t * C::Q_TILE + pn * C::Q_PANEL, &p.q_map, BAR(C::B_QFULL), 64 * pn,
+                              I.q0 + 128 * t, I.bh);
+              ++nitems;
+            }
             // K(0), then K(j+1) ahead of V(j): the order in which the MMAs read them.
             auto load = [&](const CUtensorMap* m, int j) -> bool {
               const int s = it % S;
@@ -320,7 +340,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
       // ---------------------------------------------------------- MMA issue
       {
         constexpr uint32_t idS = make_idesc(128, BN, false, false);
-        constexpr uint32_t idO = make_idesc(128, D, false, true);
+        constexpr uint32_t idO = make_idesc(128, C::PVN, false, true);
+        // O_t (+)= P V over the 16-key step k, as NPV MMAs of PVN columns each.
+        auto issue_pv = [&](int t, uint32_t p_tmem, uint32_t vb, int k, uint32_t acc) {
+#pragma unroll
+          for (int c = 0; c < C::NPV; ++c)
+            mma_ts(tmem + C::TMEM_O + t * D + c * C::PVN, p_tmem,
+                   desc_mnmajor(vb + c * (C::PVN / 64) * C::KV_PANEL, C::KV_PANEL, 16 * k), idO, acc);
+        };
         auto issue_s = [&](int t, int s) {
           const uint32_t qa = sbase + C::OFF_Q + t * C::Q_TILE;
           const uint32_t kb = sbase + C::OFF_KV + s * C::KV_TILE;
@@ -335,7 +362,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
 #pragma unroll
         for (int t = 0; t < NQ; ++t) g[t] = 0;
         bool ok = true;
-        if constexpr (C::QT) {
+        if constexpr (C::SD) {
           // Next K or V slot in load order (false if the wait gave up).
           auto take = [&](int& slot) -> bool {
             slot = it % S;
@@ -347,10 +374,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           // 16 elements of d).
           auto issue_sq = [&](int t, int b, int sk) {
             const uint32_t kb = sbase + C::OFF_KV + sk * C::KV_TILE;
+            if constexpr (C::QT) {
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k)
-              mma_ts(tmem + C::TMEM_S + (t * C::SB + b) * BN, tmem + C::TMEM_Q + t * (D / 2) + 8 * k,
-                     desc_kmajor(kb, C::KV_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+              for (int k = 0; k < D / 16; ++k)
+                mma_ts(tmem + C::TMEM_S + (t * C::SB + b) * BN, tmem + C::TMEM_Q + t * (D / 2) + 8 * k,
+                       desc_kmajor(kb, C::KV_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+            } else {
+              const uint32_t qa = sbase + C::OFF_Q + t * C::Q_TILE;
+#pragma unroll
+              for (int k = 0; k < D / 16; ++k)
+                mma_ss(tmem + C::TMEM_S + (t * C::SB + b) * BN, desc_kmajor(qa, C::Q_PANEL, 16 * k),
+                       desc_kmajor(kb, C::KV_PANEL, 16 * k), idS, k > 0 ? 1u : 0u);
+            }
             mma_commit(BAR(C::B_SFULL + t * C::SB + b));
           };
           for (int r = 0; ok; ++r) {
@@ -359,8 +394,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
             const Item I = coords(w);
             // An empty key part has no Q hand-off (the softmax warps skip it too).
             if (I.nmax <= 0) continue;
-            // The softmax warps have written this item's Q into TMEM.
-            if (!wait_warp(BAR(C::B_QREADY), nitems & 1, ab, (kKFwd << 8) | 11)) break;
+            // QT: the softmax warps have written this item's Q into TMEM; QSD: its TMA load landed.
+            if (!wait_warp(BAR(C::QT ? C::B_QREADY : C::B_QFULL), nitems & 1, ab, (kKFwd << 8) | 11)) break;
             ++nitems;
             int sk = 0;
             if (!take(sk)) break;
@@ -368,6 +403,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
             for (int t = 0; t < NQ; ++t)
               if (I.nkv[t] > 0) issue_sq(t, g[t] & 1, sk);
             mma_commit(BAR(C::B_KVEMPTY + sk));
+            if (C::QSD && I.nmax == 1) mma_commit(BAR(C::B_QEMPTY));  // the item's last S MMAs
             for (int j = 0; ok && j < I.nmax; ++j) {
               // S_t(j+1) into the other buffer of tile t, whose P_t(j-1) was read by
               // PV_t(j-1) (issued before).
@@ -380,6 +416,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
                 for (int t = 0; t < NQ; ++t)
                   if (j + 1 < I.nkv[t]) issue_sq(t, (g[t] + j + 1) & 1, sk);
                 mma_commit(BAR(C::B_KVEMPTY + sk));
+                if (C::QSD && j + 2 == I.nmax) mma_commit(BAR(C::B_QEMPTY));  // the item's last S MMAs
               }
               int sv = 0;
               if (!take(sv)) {
@@ -398,8 +435,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
-                  mma_ts(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + sb * BN + 8 * k,
-                         desc_mnmajor(vb, C::KV_PANEL, 16 * k), idO, (j > 0 || k > 0) ? 1u : 0u);
+                  issue_pv(t, tmem + C::TMEM_S + sb * BN + 8 * k, vb, k, (j > 0 || k > 0) ? 1u : 0u);
                 mma_commit(BAR(C::B_OREADY + sb));
               }
               if (!ok) break;
@@ -446,8 +482,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < BN / 16; ++k)
-                  mma_ts(tmem + C::TMEM_O + t * D, tmem + C::TMEM_S + t * BN + 8 * k,
-                         desc_mnmajor(vb, C::KV_PANEL, 16 * k), idO, (j > 0 || k > 0) ? 1u : 0u);
+                  issue_pv(t, tmem + C::TMEM_S + t * BN + 8 * k, vb, k, (j > 0 || k > 0) ? 1u : 0u);
                 mma_commit(BAR(C::B_OREADY + t));
               }
               if (j + 1 < I.nkv[t]) {
@@ -490,8 +525,8 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
       const uint32_t tO = trow + C::TMEM_O + t * D;
       const float cs = p.scale_log2;
       // Barrier and phase parity that signal completion of this tile's gm-th PV.
-      auto oready_bar = [&](int gm) { return C::QT ? t * C::SB + (gm & 1) : t; };
-      auto oready_phase = [&](int gm) -> uint32_t { return C::QT ? ((gm >> 1) & 1) : (gm & 1); };
+      auto oready_bar = [&](int gm) { return C::SD ? t * C::SB + (gm & 1) : t; };
+      auto oready_phase = [&](int gm) -> uint32_t { return C::SD ? ((gm >> 1) & 1) : (gm & 1); };
       int g = 0;  // iterations of this query tile in earlier items
       bool ok = true;
       // QT: item wq's query row r as packed bf16 pairs into TMEM lane r (the A
@@ -547,9 +582,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
         float m_used = -INFINITY;
         float l = 0.f;
         for (int j = 0; j < n; ++j) {
-          // S buffer (and its barriers) of this step: per tile, or alternating (QT).
-          const int sb = C::QT ? t * C::SB + ((g + j) & 1) : t;
-          const uint32_t sph = C::QT ? (((g + j) >> 1) & 1) : ((g + j) & 1);
+          // S buffer (and its barriers) of this step: per tile, or alternating (QT, QSD).
+          const int sb = C::SD ? t * C::SB + ((g + j) & 1) : t;
+          const uint32_t sph = C::SD ? (((g + j) >> 1) & 1) : ((g + j) & 1);
           const uint32_t tS = trow + C::TMEM_S + sb * BN;
           if (!wait_warp(BAR(C::B_SFULL + sb), sph, ab, (kKFwd << 8) | 7)) {
             ok = false;

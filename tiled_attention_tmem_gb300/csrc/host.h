@@ -84,12 +84,13 @@ size_t splitkv_workspace_bytes(int BH, int N, int d, int splits);
 int choose_splits(int BH, int N, int d, int causal);
 int fwd_launch_count(int d);
 
-// Head dims the kernels support and the head dim (64, 128 or 256) whose
+// Head dims the kernels support and the head dim (64, 128, 256 or 384) whose
 // workspace layout, preprocess and variant rules serve each: 96 runs the 128
 // kernels on zero-padded tiles; 192 has its own forward, dK/dV and dQ kernels
-// but the 256 preprocess and rules (no 5-GEMM).  0 if unsupported.
+// but the 256 preprocess and rules (no 5-GEMM); 384 has its own kernels and
+// the 7-GEMM form only.  0 if unsupported.
 inline int padded_head_dim(int d) {
-  return d == 64 ? 64 : (d == 96 || d == 128) ? 128 : (d == 192 || d == 256) ? 256 : 0;
+  return d == 64 ? 64 : (d == 96 || d == 128) ? 128 : (d == 192 || d == 256) ? 256 : d == 384 ? 384 : 0;
 }
 
 // Backward launchers (bwd.cu).  Arguments already validated; workspace sized.

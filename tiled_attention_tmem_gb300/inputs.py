@@ -90,6 +90,9 @@ HDIM256_4K = Workload("b2_h8_n4096_d256_causal_sigma0.5", 2, 8, 4096, 256, True,
 LONG_1H_16K = Workload("b1_h1_n16384_d128_causal", 1, 1, 16384, 128, True, seed=5)
 LONG_1H_8K_D256 = Workload("b1_h1_n8192_d256_causal_sigma0.5", 1, 1, 8192, 256, True,
                            seed=6, sigma=0.5, scale=1.0 / 16.0)
+# The largest head dim (lopsided tiles: 32 queries per dK/dV step, 32-key dQ tiles).
+HDIM384_4K = Workload("b2_h8_n4096_d384_causal_sigma0.5", 2, 8, 4096, 384, True,
+                      seed=7, sigma=0.5, scale=384 ** -0.5)
 
 
 def sweep_workloads() -> list[Workload]:
@@ -107,10 +110,10 @@ def sweep_workloads() -> list[Workload]:
 
 
 def head_dim_workloads() -> list[Workload]:
-    """Head-dim sweep: B=4, H=16, N=4096, d in {64, 96, 128, 192, 256}, both masks (10 points)."""
+    """Head-dim sweep: B=4, H=16, N=4096, d in {64, 96, 128, 192, 256, 384}, both masks (12 points)."""
     out = []
     k = 0
-    for d in (64, 96, 128, 192, 256):
+    for d in (64, 96, 128, 192, 256, 384):
         for causal in (False, True):
             out.append(Workload(f"hdim_n4096_d{d}{'_causal' if causal else ''}", 4, 16, 4096, d, causal,
                                 seed=200 + k))
@@ -118,7 +121,7 @@ def head_dim_workloads() -> list[Workload]:
     return out
 
 
-WORKLOADS = {w.name: w for w in [TINY, CAUSAL_2K, KSHIFT_8K, HDIM256_4K, LONG_1H_16K, LONG_1H_8K_D256]
+WORKLOADS = {w.name: w for w in [TINY, CAUSAL_2K, KSHIFT_8K, HDIM256_4K, LONG_1H_16K, LONG_1H_8K_D256, HDIM384_4K]
              + sweep_workloads() + head_dim_workloads()}
 
 
