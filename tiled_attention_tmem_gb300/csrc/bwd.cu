@@ -134,10 +134,13 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
   // Persistent grid: one CTA per SM (one fits per SM), each walking its items.
   const long long grid = std::min<long long>(items, sm_count_cached());
   const int kind = C::DQ ? FA_KERNEL_BWD_KV5 : FA_KERNEL_BWD_KV7;
-  if (qsplit <= 1)
+  // Few work items (about four per SM or fewer): the instantiation with the query
+  // split and staggered query-tile walks.
+  const bool few = qsplit > 1 || (long long)((N + C::BN - 1) / C::BN) * C::DSPLIT * BH < 4LL * sm_count_cached();
+  if (!few)
     return launch(kind, bwd_kv_kernel<C, false>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, st, p);
   fa_status s2 = launch(kind, bwd_kv_kernel<C, true>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, st, p);
-  if (s2 != FA_OK) return s2;
+  if (s2 != FA_OK || qsplit <= 1) return s2;
   KVSumParams sp{w.dkpart, w.dvpart, static_cast<uint16_t*>(dk), static_cast<uint16_t*>(dv), p.err,
                  N, Npad, BH, hd, C::D, qsplit, scale};
   const long long threads = (long long)BH * N * (hd / 8);

@@ -322,9 +322,11 @@ struct BwdKVCfg {
   static_assert(!OS || (VT && !DQ && !SEP && DSPLIT == 2), "output split: dV item and dK item per key tile");
 };
 
-// QSPLIT: the query-range split instantiation (p.qsplit > 1); the plain one
-// keeps one part per key tile as a constant and has no partial-sum epilogue.
-template <class C, bool QSPLIT>
+// FEW: the instantiation for launches with few work items (fewer than about four
+// per SM: few heads), with the query-range split (p.qsplit >= 1) and each item's
+// query-tile walk starting at its own offset; the plain one keeps one part per
+// key tile and the natural order as constants and has no partial-sum epilogue.
+template <class C, bool FEW>
 __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_constant__ BwdKVParams p) {
   constexpr int D = C::D, BM = C::BM, QS = C::QS, DH = C::DH;
   extern __shared__ uint8_t smem_raw[];
@@ -414,14 +416,14 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
   // Item w: key tile, query part and d part from the launch order; the key tile's
   // query tiles (from the diagonal under the causal mask) are cut into p.qsplit
   // contiguous parts (some possibly empty when there are fewer tiles than parts).
-  const int qsplit = QSPLIT ? p.qsplit : 1;
+  const int qsplit = FEW ? p.qsplit : 1;
   auto coords = [&](int w) {
     Item I;
     int tile;
     grouped_order(w, n_kt * C::DSPLIT * qsplit, p.BH, p.group, tile, I.bh);
     I.h = tile % C::DSPLIT;
     const int kq = tile / C::DSPLIT;
-    if constexpr (QSPLIT) {
+    if constexpr (FEW) {
       I.part = kq % qsplit;
       I.k0 = (kq / qsplit) * C::BN;
       const int first = p.causal ? I.k0 / BM : 0;
@@ -434,11 +436,13 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
       I.qt0 = p.causal ? I.k0 / BM : 0;
       I.n = n_qt - I.qt0;
     }
-    // Items of one head that run at the same time would otherwise walk the same
-    // query tiles in step (all of them from the first tile without the mask) and
-    // reduce into the same dQ rows at once; each key tile starts its walk at its
-    // own offset (n * kt / n_kt) and wraps around.
-    I.rot = I.n > 0 ? (int)((long long)I.n * (I.k0 / C::BN) / n_kt) : 0;
+    // With few heads, items of one head that run at the same time would otherwise
+    // walk the same query tiles in step (all of them from the first tile without
+    // the mask) and reduce into the same dQ rows at once; each key tile starts its
+    // walk at its own offset (n * kt / n_kt) and wraps around (measured +2 to +6 %
+    // with one to eight heads, -2.5 % with 64 heads of 2048 rows, where concurrent
+    // items belong to different heads anyway).
+    I.rot = (FEW && I.n > 0) ? (int)((long long)I.n * (I.k0 / C::BN) / n_kt) : 0;
     return I;
   };
   // Query tile of step i of item I.
@@ -764,7 +768,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           // No query of this item can see the key tile: zero gradients (zero partial
           // sums under the query-range split).
           const int c_off = C::OS ? 0 : I.h * DH;
-          if constexpr (QSPLIT) {
+          if (FEW && p.qsplit > 1) {
             if (key_ok && cw == 0) {
               const size_t off = (((size_t)I.part * p.BH + I.bh) * p.Npad + kj) * D + c_off;
               for (int c = 0; c < DH; c += 4) {
@@ -922,7 +926,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
         // item's first query tile, whose dV / dK MMAs overwrite the accumulators.
         if (!wait_warp(BAR(C::B_MMA), (g - 1) & 1, ab, (kKBwdKV << 8) | 10)) break;
         tc_fence_after();
-        if constexpr (QSPLIT) {
+        if (FEW && p.qsplit > 1) {
           // Query-range split: this part's fp32 sums (dK without the scale), one row per thread.
 #pragma unroll
           for (int which = 0; which < 2; ++which) {
