@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--variant-table", action="store_true",
                     help="time the 5-GEMM and 7-GEMM backward over a grid of shapes (one JSON line per point)")
+    ap.add_argument("--split-table", action="store_true",
+                    help="time the backward with the dK/dV query range forced to 1..8 parts (few heads)")
     ap.add_argument("--min-seconds", type=float, default=1.0,
                     help="repeat the timed pass of K steps until this long has elapsed (median pass reported)")
     return ap.parse_args()
@@ -620,10 +622,77 @@ def run_variant_table(args):
                           "auto": b.fa_bwd_choose(1, bh, n, d, int(causal))}), flush=True)
 
 
+def split_grid():
+    """(B*H, N, d, causal, variant) points of the query-split sweep: few heads (the
+    dK/dV kernel's items below two per SM), N = 2048 to 16384, both masks."""
+    pts = []
+    for d in (64, 128):
+        for causal in (True, False):
+            for n in (2048, 4096, 8192, 16384):
+                for bh in (1, 2, 4, 8, 16):
+                    if bh * (n // 128) < 304:
+                        pts.append((bh, n, d, causal, 5))
+    pts += [(1, 8192, 256, True, 7), (2, 8192, 256, True, 7), (1, 16384, 256, True, 7), (4, 4096, 256, True, 7),
+            (1, 8192, 384, True, 7), (2, 4096, 384, True, 7), (1, 8192, 192, True, 7), (1, 8192, 256, False, 7)]
+    return pts
+
+
+def run_split_table(args):
+    """Times fa_bwd at every point of split_grid() with the dK/dV kernel's query range
+    forced to 1, 2, 3, 4, 6 and 8 parts (fa_bwd_force_query_parts; CUDA events, L2
+    flushed, best of --steps calls after --warmup) and prints one JSON line per point
+    with the times and the part count the library's rule picks: the measurements the
+    rule was fitted to."""
+    import torch
+
+    from tiled_attention_tmem_gb300 import api, binding as b, build
+
+    build.build_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    gen = torch.Generator(device=dev)
+    for bh, n, d, causal, variant in split_grid():
+        gen.manual_seed(7919 * d + 31 * n + bh + (3 if causal else 0))
+        q, k, v, do = (torch.randn((1, bh, n, d), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                       for _ in range(4))
+        scale = d ** -0.5
+        o, lse = api.attention_forward(q, k, v, scale, causal)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        auto = b.fa_bwd_query_parts(1, bh, n, d, int(causal), variant)
+        ms = {}
+        for parts in (1, 2, 3, 4, 6, 8):
+            b.fa_bwd_force_query_parts(parts)
+            try:
+                ws = torch.empty(b.fa_bwd_workspace_size(1, bh, n, d, variant), dtype=torch.uint8, device=dev)
+                best = None
+                for i in range(args.warmup + args.steps):
+                    flush.fill_(float(i))
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    api.attention_backward(q, k, v, o, do, lse, scale, causal, variant=variant, workspace=ws,
+                                           grads=grads)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    if i >= args.warmup:
+                        t = e0.elapsed_time(e1)
+                        best = t if best is None else min(best, t)
+            finally:
+                b.fa_bwd_force_query_parts(0)
+            ms[parts] = best
+        api.check_device_error()
+        print(json.dumps({"BH": bh, "N": n, "d": d, "causal": causal, "variant": variant, "ms": ms,
+                          "fastest": min(ms, key=ms.get), "rule": auto}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.variant_table:
         run_variant_table(args)
+        return
+    if args.split_table:
+        run_split_table(args)
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -191,6 +191,25 @@ fa_status fa_bwd_noalloc_device_error(void* stream, int* site);
  */
 fa_status fa_bwd_noalloc_watchdog_selftest(void* stream);
 
+/*
+ * Query parts per key tile of the dK/dV kernel that fa_bwd uses for this shape
+ * and variant (1: no split).  With fewer key tiles than about two per SM (few
+ * heads) each key tile's query range is cut into parts that run as separate work
+ * items writing fp32 partial dK and dV, added by one extra kernel; the count
+ * follows a rule fitted to GB300 measurements of 1 to 8 parts.
+ */
+int fa_bwd_query_parts(int B, int H, int N, int d, int causal, int variant);
+
+/*
+ * Benchmark hook (no counterpart in the method): every later fa_bwd,
+ * fa_bwd_workspace_size and fa_bwd_launches call in this process uses `parts`
+ * query parts (1..FA_BWD_MAX_QUERY_PARTS; 0 restores the automatic choice).
+ * Set it while no fa_bwd call is in flight on any host thread and size the
+ * workspace after setting it.  FA_ERR_INVALID_ARG for other values.
+ */
+#define FA_BWD_MAX_QUERY_PARTS 16
+int fa_bwd_force_query_parts(int parts);
+
 /* The concrete variant (5 or 7) FA_BWD_AUTO runs for this shape. */
 int fa_bwd_choose(int B, int H, int N, int d, int causal);
 

@@ -270,3 +270,24 @@ def test_noalloc_source_calls_no_allocator():
     for banned in ("cudaMalloc", "cudaFree", "cuMemAlloc", "cuMemFree", "device_error_word", "malloc(",
                    "new ", "std::vector"):
         assert banned not in code, banned
+
+
+def test_query_parts_override(lib):
+    """The benchmark hook forces the dK/dV kernel's query-part count: launch count,
+    workspace and the reported count follow it, and 0 restores the automatic rule."""
+    B, H, N, d = 1, 64, 2048, 128  # many key tiles: the automatic rule does not split
+    try:
+        assert b.fa_bwd_query_parts(B, H, N, d, 1, b.FA_BWD_5GEMM) == 1
+        base_ws = b.fa_bwd_workspace_size(B, H, N, d, b.FA_BWD_5GEMM)
+        assert b.fa_bwd_launches(B, H, N, d, b.FA_BWD_5GEMM, 1) == 3
+        assert b.fa_bwd_force_query_parts(3) == b.FA_OK
+        assert b.fa_bwd_query_parts(B, H, N, d, 1, b.FA_BWD_5GEMM) == 3
+        assert b.fa_bwd_launches(B, H, N, d, b.FA_BWD_5GEMM, 1) == 4
+        # fp32 partial dK and dV for three parts
+        assert b.fa_bwd_workspace_size(B, H, N, d, b.FA_BWD_5GEMM) == base_ws + 2 * 4 * 3 * B * H * N * d
+        assert b.fa_bwd_force_query_parts(-1) == b.FA_ERR_INVALID_ARG
+        assert b.fa_bwd_force_query_parts(17) == b.FA_ERR_INVALID_ARG
+    finally:
+        assert b.fa_bwd_force_query_parts(0) == b.FA_OK
+    assert b.fa_bwd_query_parts(B, H, N, d, 1, b.FA_BWD_5GEMM) == 1
+    assert b.fa_bwd_workspace_size(B, H, N, d, b.FA_BWD_5GEMM) == base_ws

@@ -30,7 +30,8 @@ CASES = [
 
 
 def _split_used(B, H, N, d, causal, variant):
-    return b.fa_bwd_launches(B, H, N, d, variant, int(causal)) == 4
+    parts = b.fa_bwd_query_parts(B, H, N, d, int(causal), variant)
+    return parts > 1 and b.fa_bwd_launches(B, H, N, d, variant, int(causal)) == 4
 
 
 def _run(x, B, H, N, d, causal, variant):
@@ -81,3 +82,22 @@ def test_split_long_single_head_sampled_rows():
         chk = GradCheck(f"{w.name} v{variant}")
         chk.add((g[0][0, 0, qrows], g[1][0, 0, krows], g[2][0, 0, krows]), ref)
         chk.check()
+
+
+@pytest.mark.parametrize("parts", [2, 5, 8, 16])
+def test_forced_part_counts_match_oracle(parts):
+    """Every part count through the benchmark hook, including more parts than some
+    key tiles have query tiles (empty parts write zero partial sums)."""
+    B, H, N, d, causal = 1, 2, 1100, 128, True
+    x = I.make_inputs(B, H, N, d, seed=3300 + parts)
+    assert b.fa_bwd_force_query_parts(parts) == b.FA_OK
+    try:
+        assert b.fa_bwd_query_parts(B, H, N, d, 1, 5) == parts
+        got5 = _run(x, B, H, N, d, causal, 5)
+        got7 = _run(x, B, H, N, d, causal, 7)
+    finally:
+        b.fa_bwd_force_query_parts(0)
+    qf, kf, vf, dof = x.as_f64()
+    ref = oracle.backward(qf, kf, vf, dof, 1.0 / np.sqrt(d), causal)
+    check_grads(got5, ref, f"parts {parts} v5")
+    check_grads(got7, ref, f"parts {parts} v7")

@@ -45,6 +45,8 @@ SIGNATURES = {
                             _I, _I, _I, _I, _F, _I, _I, _VP]),
     "fa_bwd_noalloc_device_error": (_I, [_VP, ctypes.POINTER(_I)]),
     "fa_bwd_noalloc_watchdog_selftest": (_I, [_VP]),
+    "fa_bwd_query_parts": (_I, [_I, _I, _I, _I, _I, _I]),
+    "fa_bwd_force_query_parts": (_I, [_I]),
     "fa_bwd_choose": (_I, [_I, _I, _I, _I, _I]),
     "fa_get_device_error": (_I, [_VP, ctypes.POINTER(_I)]),
     "fa_watchdog_selftest": (_I, [_VP]),
@@ -138,6 +140,14 @@ def fa_bwd_noalloc_device_error(stream) -> tuple[int, int]:
 
 def fa_bwd_noalloc_watchdog_selftest(stream) -> int:
     return lib().fa_bwd_noalloc_watchdog_selftest(stream)
+
+
+def fa_bwd_query_parts(B, H, N, d, causal, variant) -> int:
+    return lib().fa_bwd_query_parts(B, H, N, d, int(causal), variant)
+
+
+def fa_bwd_force_query_parts(parts) -> int:
+    return lib().fa_bwd_force_query_parts(int(parts))
 
 
 def fa_bwd_choose(B, H, N, d, causal) -> int:

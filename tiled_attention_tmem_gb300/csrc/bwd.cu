@@ -1,13 +1,12 @@
 // Backward launchers: workspace carving, tile configurations and TMA descriptors.
 #include "bwd.cuh"
 #include <algorithm>
-#include <functional>
+#include <atomic>
+#include <cmath>
 #include <map>
 #include <mutex>
-#include <queue>
 #include <tuple>
 #include <type_traits>
-#include <vector>
 
 #include "host.h"
 
@@ -249,21 +248,47 @@ size_t bwd_split_bytes(int BH, int N, int d, int causal, int variant) {
   return 2 * 4 * (size_t)qsplit * BH * npad * (size_t)padded_head_dim(d);
 }
 
+namespace {
+int choose_qsplit_uncached(int BH, int N, int d, int causal, int variant) {
+  const int D = padded_head_dim(d);
+  if (D == 0 || BH <= 0 || N <= 0) return 1;
+  // d = 256 (7-GEMM): a dV item and a dK item per key tile; d = 384: three column parts.
+  const int dsplit = (variant != FA_BWD_5GEMM && D == 256) ? 2 : D == 384 ? 3 : 1;
+  const double items = (double)((N + 127) / 128) * dsplit * BH;
+  const double sms = sm_count_cached();
+  if (items >= 2.0 * sms) return 1;
+  const int cap = std::max(1, std::min(8, N / 512));
+  long parts;
+  if (causal)
+    parts = std::lround(3.0 * sms / items);
+  else if (items <= 0.42 * sms)
+    parts = std::lround(0.85 * sms / items);
+  else
+    parts = (items <= 0.85 * sms && D >= 128 && N >= 4096) ? 2 : 1;
+  return (int)std::max(1L, std::min((long)cap, parts));
+}
+std::mutex g_qsplit_mutex;
+std::map<std::tuple<int, int, int, int, int, int>, int> g_qsplit_cache;
+std::atomic<int> g_qsplit_forced{0};
+}  // namespace
+
+void force_qsplit(int parts) { g_qsplit_forced.store(parts); }
+
 // Query parts per key tile for the dK/dV kernel.  A persistent grid finishes no
 // earlier than its longest work item; with few heads there are fewer key tiles
 // than SMs, and under the causal mask the first key tile of a head sees every
 // query tile, so splitting the query range shortens the critical path at the
-// price of more item changes and a summing kernel.  The model replays the
-// kernel's dynamic claiming (items in launch order, each taken by the SM that
-// frees first) with per-query-tile and per-item costs in SM cycles, adds the
-// summing kernel's traffic, and keeps the cheapest part count.
-namespace {
-int choose_qsplit_uncached(int BH, int N, int d, int causal, int variant);
-std::mutex g_qsplit_mutex;
-std::map<std::tuple<int, int, int, int, int, int>, int> g_qsplit_cache;
-}  // namespace
-
+// price of more item changes and a summing kernel.  The rule is fitted to a
+// GB300 sweep of the part count (1, 2, 3, 4, 6, 8) over one to sixteen heads,
+// N = 2048 to 16384, head dims 64 to 384 and both masks (geometric-mean time
+// 1.05x the best measured part count, against 1.33x without splitting):
+//   - no split once the items fill two waves of SMs;
+//   - causal: about three items per SM;
+//   - no mask: about one item per SM for up to 0.42 items per SM, two parts
+//     for up to 0.85 per SM at d >= 128 and N >= 4096, else none;
+//   - at least 512 query rows per part, at most 8 parts.
 int choose_qsplit(int BH, int N, int d, int causal, int variant) {
+  if (const int forced = g_qsplit_forced.load()) return forced;
   const auto key = std::make_tuple(BH, N, d, causal, variant, sm_count_cached());
   {
     std::lock_guard<std::mutex> lock(g_qsplit_mutex);
@@ -276,56 +301,5 @@ int choose_qsplit(int BH, int N, int d, int causal, int variant) {
   g_qsplit_cache[key] = q;
   return q;
 }
-
-namespace {
-int choose_qsplit_uncached(int BH, int N, int d, int causal, int variant) {
-  const int D = padded_head_dim(d);
-  if (D == 0 || BH <= 0 || N <= 0) return 1;
-  const bool five = variant == FA_BWD_5GEMM;
-  const int bm = D == 64 ? 128 : D == 384 ? 32 : 64;  // query rows per step
-  // d = 256: a dV item and a dK item per key tile; d = 384: three column parts.
-  const int dsplit = (!five && D == 256) ? 2 : D == 384 ? 3 : 1;
-  const int n_kt = (N + 127) / 128, n_qt = (N + bm - 1) / bm;
-  const double sms = sm_count_cached();
-  if ((double)n_kt * dsplit * BH >= 2.0 * sms) return 1;
-  // GEMMs of 2 * 128 * bm * d FLOPs per item and query step
-  const double gemms = five ? 5.0 : (D == 256 ? 2.5 : D == 384 ? 2.0 + 2.0 / 3.0 : 4.0);
-  const double step = gemms * 2.0 * 128.0 * bm * d / (8192.0 * 0.55);  // cycles
-  const double item_cycles = 7000.0;
-  const double cycles_per_us = 1900.0;
-  double best_us = 0.0;
-  int best = 1;
-  const int max_parts = std::min(16, n_qt);
-  for (int parts = 1; parts <= max_parts; ++parts) {
-    // Min-heap of the SMs' next free times.
-    std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
-    for (int i = 0; i < (int)sms; ++i) free_at.push(0.0);
-    double makespan = 0.0;
-    // Launch order: key tiles first to last (under the causal mask the first is the
-    // heaviest), then parts, d parts and heads.
-    for (int kt = 0; kt < n_kt; ++kt) {
-      const int first = causal ? (kt * 128) / bm : 0;
-      const int total = n_qt - first;
-      for (int s = 0; s < parts; ++s) {
-        const int n = (int)((long long)(s + 1) * total / parts) - (int)((long long)s * total / parts);
-        const double c = n * step + item_cycles;
-        for (int h = 0; h < dsplit * BH; ++h) {
-          const double t = free_at.top() + c;
-          free_at.pop();
-          free_at.push(t);
-          makespan = std::max(makespan, t);
-        }
-      }
-    }
-    double us = makespan / cycles_per_us;
-    if (parts > 1) us += 4.0 + (double)BH * N * (2.0 * 4 * parts * D + 4.0 * d) / 6.0e6;
-    if (parts == 1 || us < 0.97 * best_us) {
-      best = parts;
-      best_us = us;
-    }
-  }
-  return best;
-}
-}  // namespace
 
 }  // namespace fa

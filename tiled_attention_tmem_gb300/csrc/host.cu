@@ -262,6 +262,19 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  (cudaStream_t)stream);
 }
 
+int fa_bwd_query_parts(int B, int H, int N, int d, int causal, int variant) {
+  if (validate_common(B, H, N, d, 1.f, causal) != FA_OK || (long long)B * H * N == 0) return 1;
+  const int v = variant == FA_BWD_AUTO ? fa_bwd_choose(B, H, N, d, causal) : variant;
+  if (!bwd_supported(d, v)) return 1;
+  return choose_qsplit(B * H, N, d, causal, v);
+}
+
+int fa_bwd_force_query_parts(int parts) {
+  if (parts < 0 || parts > FA_BWD_MAX_QUERY_PARTS) return FA_ERR_INVALID_ARG;
+  force_qsplit(parts);
+  return FA_OK;
+}
+
 fa_status fa_get_device_error(void* stream, int* site) {
   if (site) *site = 0;
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);

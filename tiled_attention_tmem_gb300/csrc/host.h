@@ -102,6 +102,8 @@ int bwd_launch_count(int BH, int N, int d, int causal, int variant);
 // Query parts per key tile of the dK/dV kernel (1: no split) and the workspace
 // bytes of its fp32 partial dK / dV (0 without a split).
 int choose_qsplit(int BH, int N, int d, int causal, int variant);
+// Benchmark hook behind fa_bwd_force_query_parts (0: the automatic choice).
+void force_qsplit(int parts);
 size_t bwd_split_bytes(int BH, int N, int d, int causal, int variant);
 
 }  // namespace fa
