@@ -261,10 +261,10 @@ int choose_qsplit_uncached(int BH, int N, int d, int causal, int variant) {
   long parts;
   if (causal)
     parts = std::lround(3.0 * sms / items);
-  else if (items <= 0.42 * sms)
-    parts = std::lround(0.85 * sms / items);
+  else if (items <= 0.85 * sms)
+    parts = std::max(2L, std::lround(0.85 * sms / items));
   else
-    parts = (items <= 0.85 * sms && D >= 128 && N >= 4096) ? 2 : 1;
+    parts = 1;
   return (int)std::max(1L, std::min((long)cap, parts));
 }
 std::mutex g_qsplit_mutex;
@@ -278,14 +278,17 @@ void force_qsplit(int parts) { g_qsplit_forced.store(parts); }
 // earlier than its longest work item; with few heads there are fewer key tiles
 // than SMs, and under the causal mask the first key tile of a head sees every
 // query tile, so splitting the query range shortens the critical path at the
-// price of more item changes and a summing kernel.  The rule is fitted to a
-// GB300 sweep of the part count (1, 2, 3, 4, 6, 8) over one to sixteen heads,
-// N = 2048 to 16384, head dims 64 to 384 and both masks (geometric-mean time
-// 1.05x the best measured part count, against 1.33x without splitting):
+// price of more item changes and a summing kernel.  (Without the mask, one long
+// item per SM of a single head also ran up to twice slower per step than the
+// same work cut in two parts, in some runs and not in others.)  The rule is
+// fitted to two GB300 sweeps of the part count (1, 2, 3, 4, 6, 8) over one to
+// sixteen heads, N = 2048 to 16384, head dims 64 to 384 and both masks, 128
+// measurements (geometric-mean time 1.07x the best measured part count,
+// against 1.37x without splitting):
 //   - no split once the items fill two waves of SMs;
 //   - causal: about three items per SM;
-//   - no mask: about one item per SM for up to 0.42 items per SM, two parts
-//     for up to 0.85 per SM at d >= 128 and N >= 4096, else none;
+//   - no mask: up to 0.85 items per SM, about one item per SM and at least two
+//     parts; none above;
 //   - at least 512 query rows per part, at most 8 parts.
 int choose_qsplit(int BH, int N, int d, int causal, int variant) {
   if (const int forced = g_qsplit_forced.load()) return forced;
