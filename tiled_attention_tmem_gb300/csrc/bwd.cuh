@@ -254,6 +254,10 @@ struct BwdKVCfg {
   // halve the per-tile critical path; the 7-GEMM kernels measured faster with one.
   static constexpr int NCW = (DQ && (EARLY || D == 64)) ? 2 : 1;
   static constexpr int CW = BM / NCW;
+  // ALLREG (7-GEMM, P^T / dS^T over S^T / dP^T, 64 query columns): all of a tile's
+  // S^T and dP^T columns are loaded with one wait, computed, then stored, instead of
+  // a load-wait round trip per 32 columns.
+  static constexpr bool ALLREG = !SEP && !EARLY && !DQ && CW == 64;
   // Without separate P^T / dS^T columns, each compute warpgroup packs its results
   // over the first half of its own S^T / dP^T columns (no warpgroup overwrites
   // columns the other still reads).  Packed column of query column c:
@@ -842,7 +846,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
               }
             }
           };
-          constexpr int HOLD = C::SEP ? C::CW / 2 : 16;
+          constexpr int HOLD = (C::SEP || C::ALLREG) ? C::CW / 2 : 16;
           uint32_t pk_p[HOLD], pk_ds[HOLD];
           // P^T = exp2(S^T c - lse2), dS^T = P^T (dP^T - D) for columns [c0, c0 + 32).
           const float2 c2 = make_float2(cs, cs);
@@ -891,6 +895,20 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
             if (lane == 0) mbar_arrive(BAR(C::B_SCONS));
 #pragma unroll
             for (int c0 = 0; c0 < C::CW; c0 += 32) compute_chunk(c_lo + c0, sr + c0, dr + c0, c0 >> 1);
+          } else if constexpr (C::ALLREG) {
+            uint32_t sr[C::CW], dr[C::CW];
+#pragma unroll
+            for (int c0 = 0; c0 < C::CW; c0 += 32) {
+              tmem_ld_32x32b_x32(trow + C::T_ST + c_lo + c0, sr + c0);
+              tmem_ld_32x32b_x32(trow + C::T_DPT + c_lo + c0, dr + c0);
+            }
+            tmem_wait_ld();
+            reg_fence<C::CW>(sr);
+            reg_fence<C::CW>(dr);
+#pragma unroll
+            for (int c0 = 0; c0 < C::CW; c0 += 32) compute_chunk(c_lo + c0, sr + c0, dr + c0, c0 >> 1);
+#pragma unroll
+            for (int c0 = 0; c0 < C::CW; c0 += 32) store_chunk(c_lo + c0, pk_p + (c0 >> 1), pk_ds + (c0 >> 1));
           } else {
 #pragma unroll
             for (int c0 = c_lo; c0 < c_lo + C::CW; c0 += 32) {
