@@ -40,11 +40,15 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum).  Keyed by the workload and the
 # hash of the kernel sources it was taken on; any source change voids it.
 NCU_TRAFFIC = {
-    ("b4_h16_n2048_d128_causal", "bwd_kv5", "30b1779b8eaf755f"): 312.9e6,
-    ("b4_h16_n2048_d128_causal", "fwd", "30b1779b8eaf755f"): 149.4e6,
-    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_kv7", "30b1779b8eaf755f"): 176.0e6,
-    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_q7", "30b1779b8eaf755f"): 195.2e6,
-    ("b2_h8_n4096_d256_causal_sigma0.5", "fwd", "30b1779b8eaf755f"): 157.8e6,
+    ("b4_h16_n2048_d128_causal", "bwd_kv5", "17fb89423f749d7a"): 311.7e6,
+    ("b4_h16_n2048_d128_causal", "fwd", "17fb89423f749d7a"): 153.5e6,
+    ("b4_h16_n2048_d128_causal", "bwd_kv7", "17fb89423f749d7a"): 170.2e6,
+    ("b4_h16_n2048_d128_causal", "bwd_q7", "17fb89423f749d7a"): 154.0e6,
+    ("b2_h16_n8192_d128_kshift3", "fwd", "17fb89423f749d7a"): 377.3e6,
+    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_kv7", "17fb89423f749d7a"): 175.1e6,
+    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_q7", "17fb89423f749d7a"): 195.6e6,
+    ("b2_h8_n4096_d256_causal_sigma0.5", "fwd", "17fb89423f749d7a"): 158.9e6,
+    ("b1_h1_n16384_d128_causal", "bwd_kv5", "17fb89423f749d7a"): 46.9e6,
 }
 
 
