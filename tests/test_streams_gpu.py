@@ -67,10 +67,20 @@ def test_two_streams_concurrently(variant):
     api.check_device_error()
 
 
-def test_cuda_graph_replay():
+GRAPH_PROBLEMS = [
+    # (B, H, N, d, causal, seed, splits): the bench-like shape, one long head with the split-KV
+    # forward and the query-split backward (extra merge and sum kernels), and head dim 384
+    (2, 4, 1024, 128, True, 31, 1),
+    (1, 1, 4096, 128, True, 33, 4),
+    (1, 2, 640, 384, True, 34, 1),
+]
+
+
+@pytest.mark.parametrize("problem", GRAPH_PROBLEMS, ids=lambda p: "b{}h{}n{}d{}".format(*p[:4]))
+def test_cuda_graph_replay(problem):
     import torch
     from tiled_attention_tmem_gb300 import api
-    B, H, N, d, causal, seed = PROBLEMS[0]
+    B, H, N, d, causal, seed, splits = problem
     q, k, v, do = _inputs(B, H, N, d, seed)
     variant = b.FA_BWD_7GEMM
     o = torch.empty_like(q)
@@ -78,8 +88,11 @@ def test_cuda_graph_replay():
     grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
     ws = torch.empty(b.fa_bwd_workspace_size(B, H, N, d, variant), dtype=torch.uint8, device=q.device)
 
+    split_ws = torch.empty(max(1, b.fa_fwd_splitkv_workspace_size(B, H, N, d, splits)), dtype=torch.uint8,
+                           device=q.device)
+
     def step():
-        api.attention_forward(q, k, v, None, causal, out=o, lse=lse)
+        api.attention_forward(q, k, v, None, causal, out=o, lse=lse, splits=splits, workspace=split_ws)
         api.attention_backward(q, k, v, o, do, lse, None, causal, variant=variant, workspace=ws, grads=grads)
 
     step()  # eager first: creates the library's device state outside the capture
