@@ -115,11 +115,13 @@ int fa_fwd_choose_splits(int B, int H, int N, int d, int causal);
  *   D (fp32 row dot products dO.O):    4*B*H*Npad bytes
  *   5-GEMM only, fp32 dQ accumulator:  4*B*H*Npad*Dk bytes (Dk = 64 or 128: the
  *                                      kernel head dim, 128 for d = 96)
- *   query-range split of the dK/dV kernel (shapes with fewer key tiles than
- *   SMs, chosen by the library's cost model for this shape and variant):
+ *   query-range split of the dK/dV kernel (shapes with fewer than about two
+ *   key tiles per SM; S = fa_bwd_query_parts for this shape and variant, the
+ *   larger over both masks):
  *                                      2*4*S*B*H*Npad*Dk bytes of fp32 partial
- *                                      dK and dV for S parts (Dk: 64, 128 or
- *                                      256), summed by one extra kernel
+ *                                      dK and dV (Dk: 64, 128, 256 or 384, the
+ *                                      kernel head dim), summed by one extra
+ *                                      kernel
  *   work-item counters:                256 bytes
  * with Npad = N rounded up to a multiple of 128.  5-GEMM: d <= 128.
  */

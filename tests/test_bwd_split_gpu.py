@@ -26,6 +26,7 @@ CASES = [
     (1, 1, 4096, 64, True, 7),
     (1, 1, 4096, 256, True, 7),
     (1, 1, 3333, 192, True, 7),
+    (1, 1, 2048, 384, True, 7),
 ]
 
 
