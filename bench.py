@@ -411,7 +411,8 @@ def run_ours(args, rank, world, local_rank):
                 "frac_of_sustained": ach / float(peaks["bf16_tflops_sustained"])}
     fwd_ms = sum(kernels[n_]["ms_avg"] for n_ in ("fwd", "fwd_merge") if n_ in kernels)
     fwd_tf = w.fwd_flops / (fwd_ms / 1e3) / 1e12 if fwd_ms else None
-    bwd_ms = sum(kernels[n_]["ms_avg"] for n_ in ("bwd_pre", "bwd_kv5", "bwd_conv", "bwd_kv7", "bwd_q7")
+    bwd_ms = sum(kernels[n_]["ms_avg"] for n_ in ("bwd_pre", "bwd_kv5", "bwd_conv", "bwd_kv7", "bwd_q7",
+                                                  "bwd_kvsum", "bwd_qsum")
                  if n_ in kernels)
     bwd_tf = w.bwd_flops / (bwd_ms / 1e3) / 1e12 if bwd_ms else None
 
@@ -457,6 +458,9 @@ def run_ours(args, rank, world, local_rank):
         "bwd_conv": 4 * bh * w.N * dk_ + 2 * bh * w.N * w.d,
         # split-KV merge: fp32 parts and their log-sum-exps read, bf16 O and LSE written
         "fwd_merge": 4 * splits * bh * w.N * (w.d + 1) + 2 * bh * w.N * w.d + 4 * bh * w.N,
+        # backward splits: fp32 partial dK and dV (dQ) of every part read, bf16 written
+        "bwd_kvsum": 2 * (4 * b.fa_bwd_query_parts(w.B, w.H, w.N, w.d, w.causal, chosen) + 2) * bh * w.N * w.d,
+        "bwd_qsum": (4 * b.fa_bwd_key_parts(w.B, w.H, w.N, w.d, w.causal, chosen) + 2) * bh * w.N * w.d,
     }
     hbm = {}
     for name_, bytes_ in hbm_bytes.items():

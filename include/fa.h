@@ -122,6 +122,11 @@ int fa_fwd_choose_splits(int B, int H, int N, int d, int causal);
  *                                      dK and dV (Dk: 64, 128, 256 or 384, the
  *                                      kernel head dim), summed by one extra
  *                                      kernel
+ *   key-range split of the 7-GEMM dQ kernel (fewer than about two query tiles
+ *   per SM; K = fa_bwd_key_parts for this shape and variant, the larger over
+ *   both masks):
+ *                                      4*K*B*H*Npad*Dk bytes of fp32 partial
+ *                                      dQ, summed by one extra kernel
  *   work-item counters:                256 bytes
  * with Npad = N rounded up to a multiple of 128.  5-GEMM: d <= 128.
  */
@@ -212,6 +217,25 @@ int fa_bwd_query_parts(int B, int H, int N, int d, int causal, int variant);
 #define FA_BWD_MAX_QUERY_PARTS 16
 int fa_bwd_force_query_parts(int parts);
 
+/*
+ * Key parts per query tile of the 7-GEMM dQ kernel that fa_bwd uses for this
+ * shape and variant (1: no split; always 1 for the 5-GEMM form, which has no dQ
+ * kernel).  With fewer query tiles than about two per SM (few heads) each query
+ * tile's key range is cut into contiguous parts that run as separate work items
+ * writing fp32 partial dQ, added in fixed order (and scaled) by one extra
+ * kernel; the count follows the query split's rule over the dQ kernel's items.
+ */
+int fa_bwd_key_parts(int B, int H, int N, int d, int causal, int variant);
+
+/*
+ * Benchmark hook like fa_bwd_force_query_parts, for the dQ kernel's key parts
+ * (1..FA_BWD_MAX_KEY_PARTS; 0 restores the automatic choice).  Same rules:
+ * set it while no fa_bwd call is in flight, size the workspace after setting
+ * it; FA_ERR_INVALID_ARG for other values.
+ */
+#define FA_BWD_MAX_KEY_PARTS 16
+int fa_bwd_force_key_parts(int parts);
+
 /* The concrete variant (5 or 7) FA_BWD_AUTO runs for this shape. */
 int fa_bwd_choose(int B, int H, int N, int d, int causal);
 
@@ -260,7 +284,8 @@ enum {
   FA_KERNEL_BWD_Q7 = 5,   /* 7-GEMM dQ kernel */
   FA_KERNEL_FWD_MERGE = 6, /* split-KV merge of the forward's parts */
   FA_KERNEL_BWD_KVSUM = 7, /* sum of the dK/dV kernel's query-range parts */
-  FA_KERNEL_KINDS = 8
+  FA_KERNEL_BWD_QSUM = 8,  /* sum of the dQ kernel's key-range parts */
+  FA_KERNEL_KINDS = 9
 };
 typedef struct {
   int launches[FA_KERNEL_KINDS];

@@ -291,3 +291,48 @@ def test_query_parts_override(lib):
         assert b.fa_bwd_force_query_parts(0) == b.FA_OK
     assert b.fa_bwd_query_parts(B, H, N, d, 1, b.FA_BWD_5GEMM) == 1
     assert b.fa_bwd_workspace_size(B, H, N, d, b.FA_BWD_5GEMM) == base_ws
+
+
+def test_key_parts_override(lib):
+    """The benchmark hook forces the dQ kernel's key-part count (7-GEMM only): launch
+    count, workspace and the reported count follow it; the 5-GEMM form has no dQ
+    kernel and stays at one part; 0 restores the automatic rule."""
+    B, H, N, d = 1, 64, 2048, 128  # many query tiles: the automatic rule does not split
+    try:
+        assert b.fa_bwd_key_parts(B, H, N, d, 1, b.FA_BWD_7GEMM) == 1
+        base7 = b.fa_bwd_workspace_size(B, H, N, d, b.FA_BWD_7GEMM)
+        base5 = b.fa_bwd_workspace_size(B, H, N, d, b.FA_BWD_5GEMM)
+        assert b.fa_bwd_launches(B, H, N, d, b.FA_BWD_7GEMM, 1) == 3
+        assert b.fa_bwd_force_key_parts(5) == b.FA_OK
+        assert b.fa_bwd_key_parts(B, H, N, d, 1, b.FA_BWD_7GEMM) == 5
+        assert b.fa_bwd_key_parts(B, H, N, d, 1, b.FA_BWD_5GEMM) == 1
+        assert b.fa_bwd_launches(B, H, N, d, b.FA_BWD_7GEMM, 1) == 4
+        assert b.fa_bwd_launches(B, H, N, d, b.FA_BWD_5GEMM, 1) == 3
+        # fp32 partial dQ for five parts; the 5-GEMM workspace is unchanged
+        assert b.fa_bwd_workspace_size(B, H, N, d, b.FA_BWD_7GEMM) == base7 + 4 * 5 * B * H * N * d
+        assert b.fa_bwd_workspace_size(B, H, N, d, b.FA_BWD_5GEMM) == base5
+        # both splits at once: both partial sums and both summing kernels
+        assert b.fa_bwd_force_query_parts(2) == b.FA_OK
+        assert b.fa_bwd_launches(B, H, N, d, b.FA_BWD_7GEMM, 1) == 5
+        assert b.fa_bwd_workspace_size(B, H, N, d, b.FA_BWD_7GEMM) == base7 + 4 * (5 + 2 * 2) * B * H * N * d
+        assert b.fa_bwd_force_key_parts(-1) == b.FA_ERR_INVALID_ARG
+        assert b.fa_bwd_force_key_parts(17) == b.FA_ERR_INVALID_ARG
+    finally:
+        assert b.fa_bwd_force_key_parts(0) == b.FA_OK
+        assert b.fa_bwd_force_query_parts(0) == b.FA_OK
+    assert b.fa_bwd_key_parts(B, H, N, d, 1, b.FA_BWD_7GEMM) == 1
+    assert b.fa_bwd_workspace_size(B, H, N, d, b.FA_BWD_7GEMM) == base7
+
+
+def test_key_split_for_few_heads(lib):
+    """Few heads under the causal mask: the dQ kernel's query tiles are far fewer
+    than the SMs, so the rule splits their key ranges (at most 8 parts, at least
+    512 keys per part), and the workspace holds the partial sums for either mask."""
+    assert b.fa_bwd_key_parts(1, 1, 4096, 256, 1, b.FA_BWD_7GEMM) == 8
+    assert b.fa_bwd_key_parts(1, 1, 1024, 256, 1, b.FA_BWD_7GEMM) == 2
+    assert b.fa_bwd_key_parts(1, 1, 4096, 128, 1, b.FA_BWD_AUTO) == 1  # AUTO: 5-GEMM, no dQ kernel
+    for causal in (0, 1):
+        k = b.fa_bwd_key_parts(1, 1, 4096, 256, causal, b.FA_BWD_7GEMM)
+        qp = b.fa_bwd_query_parts(1, 1, 4096, 256, causal, b.FA_BWD_7GEMM)
+        need = 2 * 4 * 4096 + 4 * k * 4096 * 256 + (2 * 4 * qp * 4096 * 256 if qp > 1 else 0)
+        assert b.fa_bwd_workspace_size(1, 1, 4096, 256, b.FA_BWD_7GEMM) >= need

@@ -47,6 +47,8 @@ SIGNATURES = {
     "fa_bwd_noalloc_watchdog_selftest": (_I, [_VP]),
     "fa_bwd_query_parts": (_I, [_I, _I, _I, _I, _I, _I]),
     "fa_bwd_force_query_parts": (_I, [_I]),
+    "fa_bwd_key_parts": (_I, [_I, _I, _I, _I, _I, _I]),
+    "fa_bwd_force_key_parts": (_I, [_I]),
     "fa_bwd_choose": (_I, [_I, _I, _I, _I, _I]),
     "fa_get_device_error": (_I, [_VP, ctypes.POINTER(_I)]),
     "fa_watchdog_selftest": (_I, [_VP]),
@@ -150,6 +152,14 @@ def fa_bwd_force_query_parts(parts) -> int:
     return lib().fa_bwd_force_query_parts(int(parts))
 
 
+def fa_bwd_key_parts(B, H, N, d, causal, variant) -> int:
+    return lib().fa_bwd_key_parts(B, H, N, d, int(causal), variant)
+
+
+def fa_bwd_force_key_parts(parts) -> int:
+    return lib().fa_bwd_force_key_parts(int(parts))
+
+
 def fa_bwd_choose(B, H, N, d, causal) -> int:
     return lib().fa_bwd_choose(B, H, N, d, int(causal))
 
@@ -187,7 +197,7 @@ def fa_bwd_launches(B, H, N, d, variant, causal=0) -> int:
     return lib().fa_bwd_launches(B, H, N, d, variant, int(causal))
 
 
-FA_KERNEL_KINDS = 8
+FA_KERNEL_KINDS = 9
 
 
 class FaProfile(ctypes.Structure):

@@ -48,10 +48,11 @@ struct Workspace {
   float* dqacc;
   float* dkpart;  // query-range split: fp32 partial dK, dV [qsplit][BH][Npad][d]
   float* dvpart;
+  float* dqpart;  // key-range split of the dQ kernel: fp32 partial dQ [ksplit][BH][Npad][d]
   int* sched;  // work-item counters, in the workspace's last 256 bytes
 };
 
-Workspace carve(void* ws, int BH, int Npad, int d, bool with_dq, int qsplit) {
+Workspace carve(void* ws, int BH, int Npad, int d, bool with_dq, int qsplit, int ksplit) {
   uint8_t* b = static_cast<uint8_t*>(ws);
   const size_t rows = (size_t)BH * Npad;
   Workspace w;
@@ -66,6 +67,11 @@ Workspace carve(void* ws, int BH, int Npad, int d, bool with_dq, int qsplit) {
     w.dkpart = reinterpret_cast<float*>(b + off);
     w.dvpart = reinterpret_cast<float*>(b + off + part_bytes);
     off += 2 * part_bytes;
+  }
+  w.dqpart = nullptr;
+  if (ksplit > 1) {
+    w.dqpart = reinterpret_cast<float*>(b + off);
+    off += 4 * (size_t)ksplit * rows * d;
   }
   w.sched = reinterpret_cast<int*>(b + off);
   return w;
@@ -148,7 +154,7 @@ fa_status run_kv(const void* q, const void* k, const void* v, const void* dO, co
 
 template <class C>
 fa_status run_q(const void* q, const void* k, const void* v, const void* dO, const Workspace& w, void* dq, int BH,
-                int N, int Npad, int hd, float scale, int causal, cudaStream_t st) {
+                int N, int Npad, int hd, float scale, int causal, int ksplit, cudaStream_t st) {
   BwdQParams p;
   fa_status s;
   const auto bf = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -170,15 +176,25 @@ fa_status run_q(const void* q, const void* k, const void* v, const void* dO, con
   p.scale_log2 = scale * kLog2e;
   p.scale = scale;
   p.causal = causal;
-  const int tiles = ((N + 127) / 128) * C::DQS;
+  const int tiles = ((N + 127) / 128) * C::DQS * ksplit;
   p.group = causal ? l2_head_group(12.0 * N * C::D, BH, tiles) : head_group(tiles, BH);
   p.sched = w.sched;
+  p.ksplit = ksplit;
+  p.dqpart = w.dqpart;
   const long long items = (long long)tiles * BH;
   if (items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   p.items = (int)items;
   // Persistent grid: one CTA per SM, each claiming work items.
   const long long grid = std::min<long long>(items, sm_count_cached());
-  return launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<C>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  if (ksplit <= 1)
+    return launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<C, false>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES,
+                  st, p);
+  fa_status s2 =
+      launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<C, true>, dim3((unsigned)grid), dim3(C::THREADS), C::SMEM_BYTES, st, p);
+  if (s2 != FA_OK) return s2;
+  QSumParams sp{w.dqpart, static_cast<uint16_t*>(dq), p.err, N, Npad, BH, hd, C::D, ksplit, scale};
+  const long long threads = (long long)BH * N * (hd / 8);
+  return launch(FA_KERNEL_BWD_QSUM, bwd_qsum_kernel, dim3((unsigned)((threads + 255) / 256)), dim3(256), 0, st, sp);
 }
 
 template <int D, class KV5, class KV7, class Q7>
@@ -188,7 +204,8 @@ fa_status run_d(const void* q, const void* k, const void* v, const void* o, cons
   const int Npad = (N + 127) / 128 * 128;
   const bool five = variant == FA_BWD_5GEMM;
   const int qsplit = choose_qsplit(BH, N, hd, causal, variant);
-  const Workspace w = carve(ws, BH, Npad, D, five, qsplit);
+  const int ksplit = five ? 1 : choose_ksplit(BH, N, hd, causal, variant);
+  const Workspace w = carve(ws, BH, Npad, D, five, qsplit, ksplit);
   fa_status s = run_pre<D>(o, dO, lse, w, BH, N, Npad, hd, st);
   if (s != FA_OK) return s;
   if (five) {
@@ -199,7 +216,7 @@ fa_status run_d(const void* q, const void* k, const void* v, const void* o, cons
     return FA_ERR_UNSUPPORTED;
   }
   if ((s = run_kv<KV7>(q, k, v, dO, w, dk, dv, BH, N, Npad, hd, scale, causal, qsplit, st)) != FA_OK) return s;
-  return run_q<Q7>(q, k, v, dO, w, dq, BH, N, Npad, hd, scale, causal, st);
+  return run_q<Q7>(q, k, v, dO, w, dq, BH, N, Npad, hd, scale, causal, ksplit, st);
 }
 
 }  // namespace
@@ -238,14 +255,15 @@ bool bwd_supported(int d, int variant) {
 }
 
 int bwd_launch_count(int BH, int N, int d, int causal, int variant) {
-  return 3 + (choose_qsplit(BH, N, d, causal, variant) > 1 ? 1 : 0);
+  return 3 + (choose_qsplit(BH, N, d, causal, variant) > 1 ? 1 : 0) +
+         (choose_ksplit(BH, N, d, causal, variant) > 1 ? 1 : 0);
 }
 
 size_t bwd_split_bytes(int BH, int N, int d, int causal, int variant) {
   const int qsplit = choose_qsplit(BH, N, d, causal, variant);
-  if (qsplit <= 1) return 0;
-  const size_t npad = (size_t)(N + 127) / 128 * 128;
-  return 2 * 4 * (size_t)qsplit * BH * npad * (size_t)padded_head_dim(d);
+  const int ksplit = choose_ksplit(BH, N, d, causal, variant);
+  const size_t slab = 4 * (size_t)BH * ((size_t)(N + 127) / 128 * 128) * (size_t)padded_head_dim(d);
+  return (qsplit > 1 ? 2 * (size_t)qsplit * slab : 0) + (ksplit > 1 ? (size_t)ksplit * slab : 0);
 }
 
 namespace {
@@ -270,9 +288,38 @@ int choose_qsplit_uncached(int BH, int N, int d, int causal, int variant) {
 std::mutex g_qsplit_mutex;
 std::map<std::tuple<int, int, int, int, int, int>, int> g_qsplit_cache;
 std::atomic<int> g_qsplit_forced{0};
+std::atomic<int> g_ksplit_forced{0};
+
+// The dQ kernel's key split takes the query split's rule (below) over its own
+// work items: query tiles x dQ column parts x heads.
+int choose_ksplit_uncached(int BH, int N, int d, int causal) {
+  const int D = padded_head_dim(d);
+  if (D == 0 || BH <= 0 || N <= 0) return 1;
+  const double items = (double)((N + 127) / 128) * (D == 384 ? 2 : 1) * BH;
+  const double sms = sm_count_cached();
+  if (items >= 2.0 * sms) return 1;
+  const int cap = std::max(1, std::min(8, N / 512));
+  long parts;
+  if (causal)
+    parts = std::lround(3.0 * sms / items);
+  else if (items <= 0.85 * sms)
+    parts = std::max(2L, std::lround(0.85 * sms / items));
+  else
+    parts = 1;
+  return (int)std::max(1L, std::min((long)cap, parts));
+}
 }  // namespace
 
 void force_qsplit(int parts) { g_qsplit_forced.store(parts); }
+void force_ksplit(int parts) { g_ksplit_forced.store(parts); }
+
+// Key parts per query tile of the 7-GEMM dQ kernel (1 for the 5-GEMM form, which
+// has no dQ kernel).  Cheap enough to compute per call.
+int choose_ksplit(int BH, int N, int d, int causal, int variant) {
+  if (variant == FA_BWD_5GEMM) return 1;
+  if (const int forced = g_ksplit_forced.load()) return forced;
+  return choose_ksplit_uncached(BH, N, d, causal);
+}
 
 // Query parts per key tile for the dK/dV kernel.  A persistent grid finishes no
 // earlier than its longest work item; with few heads there are fewer key tiles

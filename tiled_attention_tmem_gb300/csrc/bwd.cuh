@@ -1146,9 +1146,50 @@ struct BwdQParams {
   float scale;
   int causal;
   int group;   // heads per launch-order group
-  int items;   // work items (query tiles x heads); the grid is persistent over them
+  int items;   // work items (query tiles x key parts x dQ column parts x heads); the grid is persistent over them
   int* sched;  // [1]: next unclaimed work item (zero at launch)
+  // Key-range split (few heads, long sequences): each query tile's key tiles are
+  // cut into `ksplit` contiguous parts, each a work item of its own.  With
+  // ksplit > 1 an item writes its fp32 dQ sum over its part (without the scale)
+  // to dqpart [ksplit][BH][Npad][D] instead of dq, and bwd_qsum_kernel adds the
+  // parts.
+  int ksplit;
+  float* dqpart;
 };
+
+// Sum of the key-range parts of dQ: dQ = scale * sum_s dqpart[s] (parts in fixed
+// order, so the result is reproducible), bf16.
+struct QSumParams {
+  const float* dqpart;
+  uint16_t* dq;
+  int* err;
+  int N, Npad, BH, hd, D, parts;
+  float scale;
+};
+
+static __global__ void __launch_bounds__(256) bwd_qsum_kernel(const QSumParams p) {
+  grid_dep_wait();
+  if (*reinterpret_cast<volatile const int*>(p.err) != 0) return;
+  const int tpr = p.hd / 8;
+  const long long g = (long long)blockIdx.x * 256 + threadIdx.x;
+  const long long row = g / tpr;  // bh * N + i
+  if (row >= (long long)p.BH * p.N) return;
+  const int c = (int)(g - row * tpr) * 8;
+  const int bh = (int)(row / p.N), i = (int)(row % p.N);
+  const size_t off = ((size_t)bh * p.Npad + i) * p.D + c;
+  const size_t stride = (size_t)p.BH * p.Npad * p.D;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int s = 0; s < p.parts; ++s) {
+    const float4* q4 = reinterpret_cast<const float4*>(p.dqpart + s * stride + off);
+    const float4 x0 = q4[0], x1 = q4[1];
+    a[0] += x0.x; a[1] += x0.y; a[2] += x0.z; a[3] += x0.w;
+    a[4] += x1.x; a[5] += x1.y; a[6] += x1.z; a[7] += x1.w;
+  }
+  const float sc = p.scale;
+  *reinterpret_cast<uint4*>(p.dq + (size_t)row * p.hd + c) =
+      make_uint4(pack_bf16(a[0] * sc, a[1] * sc), pack_bf16(a[2] * sc, a[3] * sc), pack_bf16(a[4] * sc, a[5] * sc),
+                 pack_bf16(a[6] * sc, a[7] * sc));
+}
 
 // DT: dO lives in TMEM (written by the compute warps, thread = query row) and
 // dP = dO V^T takes A from TMEM; the shared memory this saves holds more K/V
@@ -1190,7 +1231,9 @@ struct BwdQCfg {
   static_assert(DQW % 64 == 0 && DQW <= 256, "dQ MMA width: whole panels, N <= 256");
 };
 
-template <class C>
+// FEW: the key-split instantiation (p.ksplit >= 1); the plain one keeps one key
+// part per query tile as a constant.
+template <class C, bool FEW>
 __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_constant__ BwdQParams p) {
   constexpr int D = C::D, BN = C::BN, S = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -1245,19 +1288,29 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
   // to the other roles through a shared-memory ring; barrier phases run on
   // across items.
   const int n_qt = (p.N + 127) / 128;
+  const int ksplit = FEW ? p.ksplit : 1;
   struct Item {
-    int q0, bh, n, h;  // first query row, head, key tiles, dQ column part
+    int q0, bh, n, h, j0, part;  // first query row, head, key tiles, dQ column part, first key tile, key part
   };
   auto coords = [&](int w) {
     Item I;
-    int qt;
-    grouped_order(w, n_qt * C::DQS, p.BH, p.group, qt, I.bh);
-    I.h = qt % C::DQS;
-    qt /= C::DQS;
+    int t;
+    grouped_order(w, n_qt * ksplit * C::DQS, p.BH, p.group, t, I.bh);
+    I.h = t % C::DQS;
+    t /= C::DQS;
+    int qt = t / ksplit;
+    I.part = t - qt * ksplit;
     if (p.causal) qt = n_qt - 1 - qt;
     I.q0 = qt * 128;
     const int last = p.causal ? min(I.q0 + 127, p.N - 1) : p.N - 1;
-    I.n = last / BN + 1;
+    const int nk = last / BN + 1;
+    if constexpr (FEW) {
+      I.j0 = (int)((long long)I.part * nk / ksplit);
+      I.n = (int)((long long)(I.part + 1) * nk / ksplit) - I.j0;
+    } else {
+      I.j0 = 0;
+      I.n = nk;
+    }
     return I;
   };
   auto item_warp = [&](int t) -> int {
@@ -1293,6 +1346,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
           const Item I = coords(wn);
           wn = atomicAdd(p.sched + 1, 1);
           if (!publish(wn)) break;
+          if (FEW && I.n == 0) continue;  // an empty key part: nothing to load or compute
           // The previous item's last S / dP MMAs must be done reading Q and dO.
           if (nitems > 0 && !wait_one(BAR(C::B_QEMPTY), (nitems - 1) & 1, ab, (kKBwdQ << 8) | 10)) break;
           mbar_expect_tx(BAR(C::B_QFULL), (C::DT ? 1 : 2) * C::Q_TILE);
@@ -1313,9 +1367,9 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
               const CUtensorMap* m = wkv ? &p.v_map : &p.k_map;
               for (int pn = 0; pn < C::PANELS; ++pn)
                 tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m, BAR(C::B_KVFULL + s),
-                            64 * pn, j * BN, I.bh);
+                            64 * pn, (I.j0 + j) * BN, I.bh);
               if (j + 4 < I.n)
-                for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(m, 64 * pn, (j + 4) * BN, I.bh);
+                for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(m, 64 * pn, (I.j0 + j + 4) * BN, I.bh);
               ++it;
             }
           }
@@ -1359,6 +1413,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
           const int w = item_warp(r);
           if (w < 0 || w >= p.items) break;
           const Item I = coords(w);
+          if (FEW && I.n == 0) continue;
           if (!wait_warp(BAR(C::B_QFULL), nitems & 1, ab, (kKBwdQ << 8) | 2)) break;
           ++nitems;
           int sk = 0, sv = 0;
@@ -1408,6 +1463,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
         const int w = item_warp(r);
         if (w < 0 || w >= p.items) break;
         const Item I = coords(w);
+        if (FEW && I.n == 0) continue;
         if (!wait_warp(BAR(C::B_QFULL), nitems & 1, ab, (kKBwdQ << 8) | 2)) break;
         ++nitems;
         for (int j = 0; ok && j < I.n; ++j, ++gj) {
@@ -1467,6 +1523,19 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
         if (w < 0 || w >= p.items) break;
         const Item I = coords(w);
         const int qi = I.q0 + r;
+        // Key-split partial sums: [part][bh][Npad][D] fp32, this row's dQ columns.
+        float* prow = nullptr;
+        if constexpr (FEW)
+          if (ksplit > 1)
+            prow = p.dqpart + (((size_t)I.part * p.BH + I.bh) * p.Npad + qi) * D + I.h * C::DQW;
+        if constexpr (FEW) {
+          if (I.n == 0) {
+            // An empty key part contributes zeros to the sum.
+            if (prow != nullptr)
+              for (int c = 0; c < C::DQW; c += 4) *reinterpret_cast<float4*>(prow + c) = make_float4(0.f, 0.f, 0.f, 0.f);
+            continue;
+          }
+        }
         const float l2 = p.lse2[(size_t)I.bh * p.Npad + qi];  // -inf past N: every p is 0
         const float dd = p.dd[(size_t)I.bh * p.Npad + qi];
         const float2 l22 = make_float2(l2, l2), dd2 = make_float2(dd, dd);
@@ -1502,7 +1571,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
             break;
           }
           tc_fence_after();
-          const int kbase = j * BN;
+          const int kbase = (I.j0 + j) * BN;
           // P = exp2(S c - lse2) and dS = P (dP - D) for columns [c0, c0 + 32),
           // packed to bf16 over the first half of dP's columns (chunk c0 -> c0 / 2).
           auto ds_chunk = [&](int c0, const uint32_t* sr, const uint32_t* dr) {
@@ -1560,6 +1629,26 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
         // the next item's first key tile, whose dQ MMA overwrites the accumulator.
         if (!wait_warp(BAR(C::B_DQ), (gj - 1) & 1, ab, (kKBwdQ << 8) | 6)) break;
         tc_fence_after();
+        if constexpr (FEW) {
+          if (prow != nullptr) {
+            // Unscaled fp32 partial of this key part, every row of the tile (rows
+            // past N are zero and never summed).
+#pragma unroll
+            for (int c0 = 0; c0 < C::DQW; c0 += 32) {
+              uint32_t rv[32];
+              tmem_ld_32x32b_x32(trow + C::T_DQ + c0, rv);
+              tmem_wait_ld();
+              reg_fence<32>(rv);
+              float4* d4 = reinterpret_cast<float4*>(prow + c0);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                d4[v] = make_float4(__uint_as_float(rv[4 * v]), __uint_as_float(rv[4 * v + 1]),
+                                    __uint_as_float(rv[4 * v + 2]), __uint_as_float(rv[4 * v + 3]));
+            }
+            tc_fence_before();
+            continue;
+          }
+        }
         const int row0 = I.q0 + quad * 32;
         uint16_t* obase = p.dq + ((size_t)I.bh * p.N + (size_t)row0) * p.hd + I.h * C::DQW;
         const int hd_left = p.hd - I.h * C::DQW;  // columns of this part inside the head dim

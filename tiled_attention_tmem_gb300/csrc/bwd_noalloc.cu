@@ -148,11 +148,13 @@ fa_status run(const void* q, const void* k, const void* v, const void* o, const 
   const int q_tiles = ((N + 127) / 128) * Q7::DQS;
   qp.group = causal ? l2_head_group(12.0 * N * D, BH, q_tiles) : head_group(q_tiles, BH);
   qp.sched = sched;
+  qp.ksplit = 1;  // no key-range split: its partial sums would need more scratch
+  qp.dqpart = nullptr;
   const long long q_items = (long long)q_tiles * BH;
   if (q_items > 0x7fffffffLL) return FA_ERR_INVALID_ARG;
   qp.items = (int)q_items;
   const long long q_grid = std::min<long long>(q_items, sm_count_cached());
-  return launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<Q7>, dim3((unsigned)q_grid), dim3(Q7::THREADS), Q7::SMEM_BYTES,
+  return launch(FA_KERNEL_BWD_Q7, bwd_q_kernel<Q7, false>, dim3((unsigned)q_grid), dim3(Q7::THREADS), Q7::SMEM_BYTES,
                 st, qp);
 }
 

@@ -279,6 +279,19 @@ int fa_bwd_force_query_parts(int parts) {
   return FA_OK;
 }
 
+int fa_bwd_key_parts(int B, int H, int N, int d, int causal, int variant) {
+  if (validate_common(B, H, N, d, 1.f, causal) != FA_OK || (long long)B * H * N == 0) return 1;
+  const int v = variant == FA_BWD_AUTO ? fa_bwd_choose(B, H, N, d, causal) : variant;
+  if (!bwd_supported(d, v)) return 1;
+  return choose_ksplit(B * H, N, d, causal, v);
+}
+
+int fa_bwd_force_key_parts(int parts) {
+  if (parts < 0 || parts > FA_BWD_MAX_KEY_PARTS) return FA_ERR_INVALID_ARG;
+  force_ksplit(parts);
+  return FA_OK;
+}
+
 fa_status fa_get_device_error(void* stream, int* site) {
   if (site) *site = 0;
   cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
@@ -355,6 +368,7 @@ const char* fa_kernel_name(int kind) {
     case FA_KERNEL_BWD_Q7: return "bwd_q7";
     case FA_KERNEL_FWD_MERGE: return "fwd_merge";
     case FA_KERNEL_BWD_KVSUM: return "bwd_kvsum";
+    case FA_KERNEL_BWD_QSUM: return "bwd_qsum";
   }
   return "unknown";
 }

@@ -100,10 +100,14 @@ fa_status run_bwd(const void* q, const void* k, const void* v, const void* o, co
 bool bwd_supported(int d, int variant);
 int bwd_launch_count(int BH, int N, int d, int causal, int variant);
 // Query parts per key tile of the dK/dV kernel (1: no split) and the workspace
-// bytes of its fp32 partial dK / dV (0 without a split).
+// bytes of the fp32 partials of both splits (0 without a split).
 int choose_qsplit(int BH, int N, int d, int causal, int variant);
 // Benchmark hook behind fa_bwd_force_query_parts (0: the automatic choice).
 void force_qsplit(int parts);
+// Key parts per query tile of the 7-GEMM dQ kernel (1: no split; always 1 for the
+// 5-GEMM form) and its benchmark hook behind fa_bwd_force_key_parts.
+int choose_ksplit(int BH, int N, int d, int causal, int variant);
+void force_ksplit(int parts);
 size_t bwd_split_bytes(int BH, int N, int d, int causal, int variant);
 
 }  // namespace fa
