@@ -68,6 +68,8 @@ def parse_args():
                     help="time the 5-GEMM and 7-GEMM backward over a grid of shapes (one JSON line per point)")
     ap.add_argument("--split-table", action="store_true",
                     help="time the backward with the dK/dV query range forced to 1..8 parts (few heads)")
+    ap.add_argument("--key-split-table", action="store_true",
+                    help="time the 7-GEMM backward with the dQ kernel's key range forced to 1..12 parts (few heads)")
     ap.add_argument("--min-seconds", type=float, default=1.0,
                     help="repeat the timed pass of K steps until this long has elapsed (median pass reported)")
     return ap.parse_args()
@@ -694,8 +696,76 @@ def run_split_table(args):
                           "fastest": min(ms, key=ms.get), "rule": auto}), flush=True)
 
 
+def key_split_grid():
+    """(B*H, N, d, causal) points of the key-split sweep: the 7-GEMM dQ kernel's work
+    items (query tiles x dQ column parts x heads) below two per SM, N = 2048 to 16384,
+    d = 64 to 384, both masks."""
+    pts = []
+    for d in (64, 128, 192, 256, 384):
+        dqs = 2 if d == 384 else 1
+        for causal in (True, False):
+            for n in (2048, 4096, 8192, 16384):
+                for bh in (1, 2, 4, 8, 16):
+                    if bh * (n // 128) * dqs < 304 and not (d == 384 and n == 16384):
+                        pts.append((bh, n, d, causal))
+    return pts
+
+
+def run_key_split_table(args):
+    """Times the 7-GEMM fa_bwd at every point of key_split_grid() with the dQ kernel's
+    key range forced to 1, 2, 3, 4, 6, 8 and 12 parts (fa_bwd_force_key_parts; the
+    query split left to the library; CUDA events, L2 flushed, best of --steps calls
+    after --warmup) and prints one JSON line per point with the times and the part
+    count the library's rule picks."""
+    import torch
+
+    from tiled_attention_tmem_gb300 import api, binding as b, build
+
+    build.build_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    gen = torch.Generator(device=dev)
+    for bh, n, d, causal in key_split_grid():
+        gen.manual_seed(7907 * d + 29 * n + bh + (5 if causal else 0))
+        q, k, v, do = (torch.randn((1, bh, n, d), generator=gen, device=dev, dtype=torch.float32).to(torch.bfloat16)
+                       for _ in range(4))
+        scale = d ** -0.5
+        o, lse = api.attention_forward(q, k, v, scale, causal)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        auto = b.fa_bwd_key_parts(1, bh, n, d, int(causal), b.FA_BWD_7GEMM)
+        ms = {}
+        for parts in (1, 2, 3, 4, 6, 8, 12):
+            b.fa_bwd_force_key_parts(parts)
+            try:
+                ws = torch.empty(b.fa_bwd_workspace_size(1, bh, n, d, b.FA_BWD_7GEMM), dtype=torch.uint8,
+                                 device=dev)
+                best = None
+                for i in range(args.warmup + args.steps):
+                    flush.fill_(float(i))
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    api.attention_backward(q, k, v, o, do, lse, scale, causal, variant=b.FA_BWD_7GEMM,
+                                           workspace=ws, grads=grads)
+                    e1.record(stream)
+                    torch.cuda.synchronize()
+                    if i >= args.warmup:
+                        t = e0.elapsed_time(e1)
+                        best = t if best is None else min(best, t)
+            finally:
+                b.fa_bwd_force_key_parts(0)
+            ms[parts] = best
+        api.check_device_error()
+        print(json.dumps({"BH": bh, "N": n, "d": d, "causal": causal, "ms": ms,
+                          "fastest": min(ms, key=ms.get), "rule": auto}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.key_split_table:
+        run_key_split_table(args)
+        return
     if args.variant_table:
         run_variant_table(args)
         return
