@@ -1357,6 +1357,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_q_kernel(const __grid_const
           }
           ++nitems;
           for (int j = 0; j < I.n && ok; ++j) {
+            // The next item's Q and dO into L2 a few key steps before this item ends.
+            if (j == max(0, I.n - 3) && wn < p.items) {
+              const Item J = coords(wn);
+              if (!FEW || J.n > 0)
+                for (int pn = 0; pn < C::PANELS; ++pn) {
+                  tma_prefetch_l2_3d(&p.q_map, 64 * pn, J.q0, J.bh);
+                  tma_prefetch_l2_3d(&p.do_map, 64 * pn, J.q0, J.bh);
+                }
+            }
             for (int wkv = 0; wkv < 2; ++wkv) {
               const int s = it % S;
               if (!wait_one(BAR(C::B_KVEMPTY + s), ((it / S) & 1) ^ 1, ab, (kKBwdQ << 8) | 1)) {

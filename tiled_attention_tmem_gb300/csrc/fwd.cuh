@@ -91,6 +91,7 @@ struct FwdCfg {
   static constexpr int PVN = D / NPV;
   static constexpr int BM = 128;
   static constexpr int PREFETCH = STAGES / 2 + 2;  // K/V tiles ahead for L2 prefetch
+  static constexpr int QPF = 3;  // key steps before an item's end at which the next item's Q is prefetched
   static constexpr int PANELS = D / 64;
   static constexpr uint32_t Q_PANEL = BM * 128;
   static constexpr uint32_t Q_TILE = PANELS * Q_PANEL;
@@ -270,6 +271,18 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           if (w >= p.items) break;
           const Item I = coords(w);
           const Part P = part_of(w);
+          // The next item's Q tiles into L2 a few key steps before this item ends,
+          // so that its load (or, with Q in TMEM, the softmax warps' row reads)
+          // at the item change is served from L2.
+          auto prefetch_next_q = [&](int j) {
+            if (j != max(0, I.nmax - C::QPF)) return;
+            const int w2 = item_of(r + 1);
+            if (w2 >= p.items) return;
+            const Item J = coords(w2);
+            for (int t = 0; t < NQ; ++t)
+              if (J.q0 + 128 * t < p.N)
+                for (int pn = 0; pn < C::PANELS; ++pn) tma_prefetch_l2_3d(&p.q_map, 64 * pn, J.q0 + 128 * t, J.bh);
+          };
           if constexpr (C::SD) {
             if (C::QSD && I.nmax > 0) {
               // This item's Q, once the previous item's S MMAs are done reading Q.
@@ -297,6 +310,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
             };
             if (I.nmax > 0) ok = load(&p.k_map, 0);
             for (int j = 0; j < I.nmax && ok; ++j) {
+              prefetch_next_q(j);
               if (j + 1 < I.nmax) ok = load(&p.k_map, j + 1);
               if (ok) ok = load(&p.v_map, j);
             }
@@ -312,6 +326,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
                           I.q0 + 128 * t, I.bh);
           ++nitems;
           for (int j = 0; j < I.nmax && ok; ++j) {
+            prefetch_next_q(j);
             for (int wkv = 0; wkv < 2; ++wkv) {
               const int s = it % S;
               if (!wait_one(BAR(C::B_KVEMPTY + s), ((it / S) & 1) ^ 1, ab, (kKFwd << 8) | 1)) {
