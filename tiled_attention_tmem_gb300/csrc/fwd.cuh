@@ -266,6 +266,15 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
         tma_prefetch_desc(&p.v_map);
         int it = 0, nitems = 0;
         bool ok = true;
+        // No L2 prefetches until the CTA's first K tile has landed (at the start
+        // every CTA loads at once; prefetches then only delay the first tiles).
+        // Slot 0 has seen one load until more than S were issued, and the (S+1)-th
+        // waited for the first to be consumed.
+        bool warm = false;
+        auto is_warm = [&]() -> bool {
+          if (!warm) warm = it > S || (it >= 1 && mbar_test(BAR(C::B_KVFULL), 0));
+          return warm;
+        };
         for (int r = 0; ok; ++r) {
           const int w = item_of(r);
           if (w >= p.items) break;
@@ -275,7 +284,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
           // so that its load (or, with Q in TMEM, the softmax warps' row reads)
           // at the item change is served from L2.
           auto prefetch_next_q = [&](int j) {
-            if (j != max(0, I.nmax - C::QPF)) return;
+            if (j != max(0, I.nmax - C::QPF) || !is_warm()) return;
             const int w2 = item_of(r + 1);
             if (w2 >= p.items) return;
             const Item J = coords(w2);
@@ -302,7 +311,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
               for (int pn = 0; pn < C::PANELS; ++pn)
                 tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m, BAR(C::B_KVFULL + s),
                             64 * pn, (P.lo + j) * BN, I.bh);
-              if (j + C::PREFETCH < I.nmax)
+              if (j + C::PREFETCH < I.nmax && is_warm())
                 for (int pn = 0; pn < C::PANELS; ++pn)
                   tma_prefetch_l2_3d(m, 64 * pn, (P.lo + j + C::PREFETCH) * BN, I.bh);
               ++it;
@@ -339,7 +348,7 @@ __global__ void __launch_bounds__(C::THREADS, 1) fwd_kernel(const __grid_constan
                 tma_load_3d(sbase + C::OFF_KV + s * C::KV_TILE + pn * C::KV_PANEL, m, BAR(C::B_KVFULL + s),
                             64 * pn, (P.lo + j) * BN, I.bh);
               // Pull K/V tiles a few steps beyond the ring into L2.
-              if (j + C::PREFETCH < I.nmax)
+              if (j + C::PREFETCH < I.nmax && is_warm())
                 for (int pn = 0; pn < C::PANELS; ++pn)
                   tma_prefetch_l2_3d(m, 64 * pn, (P.lo + j + C::PREFETCH) * BN, I.bh);
               ++it;
