@@ -230,11 +230,13 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d, int variant) {
 
 // Measured on GB300 (bench.py --variant-table: 306 shapes, d = 64, 96 and 128,
 // both masks, 1 to 512 heads, N = 512 to 16384, each form with its own
-// few-heads query split; two runs): the 5-GEMM form was faster at 305 of 306
-// points in each run, with the 7-GEMM form taking 1.04x to 2.6x its time
-// (median 1.3x); the single exception differed between the runs (0.2 % and
-// 14 % ahead at one small shape each).  So AUTO takes the 5-GEMM form wherever
-// it exists (d <= 128); d = 192, 256 and 384 have only the 7-GEMM form.
+// few-heads splits; three runs): the 5-GEMM form was faster at 305, 305 and 299
+// of 306 points, with the 7-GEMM form taking up to 2.6x its time (median 1.3x).
+// The exceptions differed between the runs; those of the third (up to 23 %
+// ahead, without the mask at 32 or 64 key tiles) were runs of the 5-GEMM form's
+// slow mode at those shapes, and timed again the 5-GEMM form was ahead at each.
+// So AUTO takes the 5-GEMM form wherever it exists (d <= 128); d = 192, 256 and
+// 384 have only the 7-GEMM form.
 int fa_bwd_choose(int B, int H, int N, int d, int causal) {
   (void)B;
   (void)H;
