@@ -17,9 +17,12 @@ from helpers import TOL_GRAD_REL, to_dev
 pytestmark = pytest.mark.gpu
 
 PROBLEMS = [
-    # (B, H, N, d, causal, seed)
+    # (B, H, N, d, causal, seed); the last is one head of 2048 rows, where the backward
+    # splits the dK/dV kernel's query ranges (and, 7-GEMM, the dQ kernel's key ranges)
+    # with partial sums in the caller's workspace
     (2, 4, 1024, 128, True, 31),
     (1, 8, 768, 64, False, 32),
+    (1, 1, 2048, 128, True, 35),
 ]
 
 
