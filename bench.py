@@ -40,19 +40,19 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # (dram__bytes_read.sum + dram__bytes_write.sum).  Keyed by the workload and the
 # hash of the kernel sources it was taken on; any source change voids it.
 NCU_TRAFFIC = {
-    ("b4_h16_n2048_d128_causal", "bwd_kv5", "43061831af124547"): 312.0e6,
-    ("b4_h16_n2048_d128_causal", "fwd", "43061831af124547"): 157.9e6,
-    ("b4_h16_n2048_d128_causal", "bwd_kv7", "43061831af124547"): 170.3e6,
-    ("b4_h16_n2048_d128_causal", "bwd_q7", "43061831af124547"): 154.6e6,
-    ("b2_h16_n8192_d128_kshift3", "fwd", "43061831af124547"): 359.8e6,
-    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_kv7", "43061831af124547"): 175.1e6,
-    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_q7", "43061831af124547"): 197.8e6,
-    ("b2_h8_n4096_d256_causal_sigma0.5", "fwd", "43061831af124547"): 155.7e6,
-    ("b1_h1_n16384_d128_causal", "bwd_kv5", "43061831af124547"): 46.7e6,
-    ("b1_h1_n8192_d256_causal_sigma0.5", "bwd_q7", "43061831af124547"): 22.3e6,
-    ("b1_h1_n8192_d256_causal_sigma0.5", "bwd_kv7", "43061831af124547"): 28.7e6,
-    ("b2_h16_n8192_d128_kshift3", "bwd_kv5", "43061831af124547"): 944.4e6,
-    ("b2_h8_n4096_d384_causal_sigma0.5", "bwd_kv7", "43061831af124547"): 280.0e6,
+    ("b4_h16_n2048_d128_causal", "bwd_kv5", "bdd7365a73e89c76"): 310.8e6,
+    ("b4_h16_n2048_d128_causal", "fwd", "bdd7365a73e89c76"): 156.6e6,
+    ("b4_h16_n2048_d128_causal", "bwd_kv7", "bdd7365a73e89c76"): 170.7e6,
+    ("b4_h16_n2048_d128_causal", "bwd_q7", "bdd7365a73e89c76"): 154.6e6,
+    ("b2_h16_n8192_d128_kshift3", "fwd", "bdd7365a73e89c76"): 377.4e6,
+    ("b2_h16_n8192_d128_kshift3", "bwd_kv5", "bdd7365a73e89c76"): 943.9e6,
+    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_kv7", "bdd7365a73e89c76"): 175.8e6,
+    ("b2_h8_n4096_d256_causal_sigma0.5", "bwd_q7", "bdd7365a73e89c76"): 197.8e6,
+    ("b2_h8_n4096_d256_causal_sigma0.5", "fwd", "bdd7365a73e89c76"): 159.5e6,
+    ("b2_h8_n4096_d384_causal_sigma0.5", "bwd_kv7", "bdd7365a73e89c76"): 280.0e6,
+    ("b1_h1_n16384_d128_causal", "bwd_kv5", "bdd7365a73e89c76"): 46.7e6,
+    ("b1_h1_n8192_d256_causal_sigma0.5", "bwd_q7", "bdd7365a73e89c76"): 22.3e6,
+    ("b1_h1_n8192_d256_causal_sigma0.5", "bwd_kv7", "bdd7365a73e89c76"): 29.0e6,
 }
 
 

@@ -496,11 +496,17 @@ __global__ void __launch_bounds__(C::THREADS, 1) bwd_kv_kernel(const __grid_cons
           ++published;
           return true;
         };
-        int wn = atomicAdd(p.sched, 1);
+        // 5-GEMM: the first item of CTA c is item c (the grid never exceeds the
+        // items) and the counter hands out the rest, so no CTA starts behind a
+        // contended atomic (measured -1 % on 64 heads of 2048 rows, -4 % on one
+        // head of 16384; the 7-GEMM kernels measured 1 % slower with it at d = 256
+        // and claim every item).
+        const int first = C::DQ ? (int)gridDim.x : 0;
+        int wn = C::DQ ? (int)blockIdx.x : atomicAdd(p.sched, 1);
         ok = publish(wn);
         while (ok && wn < p.items) {
           const int w = wn;
-          wn = atomicAdd(p.sched, 1);
+          wn = first + atomicAdd(p.sched, 1);
           if (!publish(wn)) break;
           const Item I = coords(w);
           if (I.n <= 0) continue;
